@@ -1,0 +1,343 @@
+"""Pins for the CPU oracle: each check is independent of the oracle's own code.
+
+* non-absorbed multi-head attention with random up-projections (the form the
+  absorbed decode is derived from) must equal the absorbed result;
+* closed forms (one key; all keys scored equally; a hand-derived two-token
+  golden case);
+* the split-KV pieces merged by log-sum-exp equal the unsplit result;
+* a pure-Python brute force with its own gather, math.fsum and a softmax
+  without max subtraction;
+* torch's float8_e4m3fn decoder for every E4M3 code;
+* causal masking of two draft positions against single-position calls;
+* page relabelling, prefix copies and tail sentinels leave the result alone.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import attend, lse_merge, mla_decode_ref, mla_decode_ref_pieces
+from paged_mla_decode_09_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- encodings
+def test_e4m3_table_matches_torch():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = oracle.e4m3_to_f64(codes)
+    assert np.array_equal(np.isnan(ref), np.isnan(mine))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], mine[ok])
+
+
+def test_e4m3_extremes():
+    t = oracle.e4m3_decode_table()
+    assert t[0x7E] == 448.0 and t[0xFE] == -448.0
+    assert t[0x01] == 2.0**-9  # smallest subnormal
+    assert t[0x08] == 2.0**-6  # smallest normal
+    assert t[0x38] == 1.0
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert np.sum(np.isnan(t)) == 2
+    assert t[0x80] == 0.0 and math.copysign(1.0, t[0x80]) == -1.0
+
+
+def test_bf16_decode_patterns():
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x3E80, 0x4049], dtype=np.uint16)
+    v = oracle.bf16_bits_to_f64(bits)
+    assert list(v[:4]) == [1.0, -2.0, 0.0, 0.25]
+    assert v[4] == 3.140625
+
+
+def test_generator_bf16_rounding_is_nearest_even():
+    x = np.array([1.0 + 2.0**-8, 1.0 + 3 * 2.0**-8, 1.0 + 2.0**-9], dtype=np.float32)
+    bits = W.f32_to_bf16_bits(x)
+    # 1+2^-8 is a tie between 1 and 1+2^-7 -> even (1); 1+3*2^-8 ties -> 1+2^-6
+    assert list(oracle.bf16_bits_to_f64(bits)) == [1.0, 1.0 + 2.0**-6, 1.0]
+
+
+# ----------------------------------------------- non-absorbed equivalence
+def _mha_nonabsorbed(q_h, q_pe, c, k_pe, w_uk, w_uv, nvis, scale):
+    """Standard attention with decompressed keys/values for one head."""
+    K = np.concatenate([c @ w_uk.T, k_pe], axis=1)  # [L, 128 + 64]
+    V = c @ w_uv.T  # [L, 128]
+    q = np.concatenate([q_h, q_pe])
+    s = (K[:nvis] @ q) * scale
+    m = s.max()
+    p = np.exp(s - m)
+    z = p.sum()
+    return (p / z) @ V[:nvis], m + np.log(z)
+
+
+def test_non_absorbed_equivalence_dense_weights():
+    rng = np.random.default_rng(11)
+    H, L, dh = 4, 37, 128
+    scale = 1 / math.sqrt(192)
+    c = rng.standard_normal((L, 512))
+    k_pe = rng.standard_normal((L, 64))
+    rows = np.concatenate([c, k_pe], axis=1)
+    qrows, expect = [], []
+    for h in range(H):
+        w_uk = rng.standard_normal((dh, 512)) / math.sqrt(512)
+        w_uv = rng.standard_normal((dh, 512)) / math.sqrt(512)
+        q_h = rng.standard_normal(dh)
+        q_pe = rng.standard_normal(64)
+        qrows.append((np.concatenate([w_uk.T @ q_h, q_pe]), w_uv))
+        expect.append(_mha_nonabsorbed(q_h, q_pe, c, k_pe, w_uk, w_uv, L, scale))
+    out, lse = attend(np.stack([q for q, _ in qrows]), rows, L, scale)
+    for h in range(H):
+        w_uv = qrows[h][1]
+        np.testing.assert_allclose(w_uv @ out[h], expect[h][0], rtol=1e-10, atol=1e-12)
+        assert abs(lse[h] - expect[h][1]) <= 1e-10 * max(1.0, abs(expect[h][1]))
+
+
+def test_non_absorbed_equivalence_through_paged_bf16_entry():
+    """End to end through the bf16 entry point: W_UK maps every latent
+    coordinate to one signed coordinate of q_h, so the absorbed query is
+    exactly representable in bf16; W_UV is dense."""
+    rng = np.random.default_rng(5)
+    H, dh = 3, 128
+    wl = W.custom([150], num_heads=H, seed=77)
+    L = int(wl.seq_lens[0])
+    rows = oracle.decode_cache_rows(oracle.gather_rows(wl.kv_cache, wl.page_table[0], L), "bf16", 1.0)
+    c, k_pe = rows[:, :512], rows[:, 512:]
+    q_pe = oracle.bf16_bits_to_f64(wl.q_pe[0, 0])
+    qn_bits = np.empty((1, 1, H, 512), dtype=np.uint16)
+    expect = []
+    for h in range(H):
+        q_h_bits = W.f32_to_bf16_bits(rng.standard_normal(dh).astype(np.float32))
+        q_h = oracle.bf16_bits_to_f64(q_h_bits)
+        pi = rng.integers(0, dh, size=512)
+        sg = rng.choice([-1.0, 1.0], size=512)
+        w_uk = np.zeros((dh, 512))
+        w_uk[pi, np.arange(512)] = sg
+        qn = w_uk.T @ q_h  # each entry = +-q_h[pi[j]], exact in bf16
+        qn_bits[0, 0, h] = W.f32_to_bf16_bits(qn.astype(np.float32))
+        assert np.array_equal(oracle.bf16_bits_to_f64(qn_bits[0, 0, h]), qn)
+        w_uv = rng.standard_normal((dh, 512)) / math.sqrt(512)
+        expect.append((w_uv, _mha_nonabsorbed(q_h, q_pe[h], c, k_pe, w_uk, w_uv, L, wl.scale)))
+    out, lse = mla_decode_ref(qn_bits, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 1, wl.scale)
+    for h in range(H):
+        w_uv, (o_ref, lse_ref) = expect[h]
+        np.testing.assert_allclose(w_uv @ out[0, 0, h], o_ref, rtol=1e-10, atol=1e-12)
+        assert abs(lse[0, 0, h] - lse_ref) <= 1e-10 * max(1.0, abs(lse_ref))
+
+
+# ------------------------------------------------------------ closed forms
+def test_single_key_returns_its_latent_row():
+    wl = W.custom([1], num_heads=4, seed=3)
+    out, lse = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 1, wl.scale)
+    row = oracle.bf16_bits_to_f64(wl.kv_cache[wl.page_table[0, 0], 0])
+    for h in range(4):
+        assert np.array_equal(out[0, 0, h], row[:512])
+        q = np.concatenate([oracle.bf16_bits_to_f64(wl.q_nope[0, 0, h]), oracle.bf16_bits_to_f64(wl.q_pe[0, 0, h])])
+        assert abs(lse[0, 0, h] - wl.scale * math.fsum(q * row)) < 1e-12
+
+
+def test_zero_query_gives_mean_and_log_count():
+    wl = W.custom([70, 129], num_heads=2, seed=4)
+    zn = np.zeros_like(wl.q_nope)
+    zp = np.zeros_like(wl.q_pe)
+    out, lse = mla_decode_ref(zn, zp, wl.kv_cache, wl.page_table, wl.seq_lens, 1, wl.scale)
+    for b in range(2):
+        L = int(wl.seq_lens[b])
+        rows = oracle.bf16_bits_to_f64(oracle.gather_rows(wl.kv_cache, wl.page_table[b], L))
+        mean = np.array([math.fsum(rows[:, d]) / L for d in range(512)])
+        np.testing.assert_allclose(out[b, 0, 0], mean, rtol=0, atol=1e-13)
+        assert abs(lse[b, 0, 1] - math.log(L)) < 1e-13
+
+
+def test_equal_scores_from_rope_only():
+    """q_nope = 0 and every k_pe identical: all scores equal s, so the output
+    is the mean latent row and lse = s + ln L."""
+    wl = W.custom([91], num_heads=2, seed=6)
+    cache = wl.kv_cache.copy()
+    pe = W.f32_to_bf16_bits(np.linspace(-1, 1, 64).astype(np.float32))
+    for p in range(cache.shape[0]):
+        cache[p, :, 512:] = pe
+    zn = np.zeros_like(wl.q_nope)
+    out, lse = mla_decode_ref(zn, wl.q_pe, cache, wl.page_table, wl.seq_lens, 1, wl.scale)
+    L = 91
+    rows = oracle.bf16_bits_to_f64(oracle.gather_rows(cache, wl.page_table[0], L))
+    mean = rows[:, :512].mean(axis=0)
+    for h in range(2):
+        s = wl.scale * math.fsum(oracle.bf16_bits_to_f64(wl.q_pe[0, 0, h]) * oracle.bf16_bits_to_f64(pe))
+        np.testing.assert_allclose(out[0, 0, h], mean, rtol=0, atol=1e-13)
+        assert abs(lse[0, 0, h] - (s + math.log(L))) < 1e-12
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = float(v)
+    return vals
+
+
+def test_golden_two_token_logistic():
+    g = _read_golden("two_token_logistic.txt")
+    one, two = np.uint16(0x3F80), np.uint16(0x4000)
+    qn = np.zeros((1, 1, 1, 512), dtype=np.uint16)
+    qn[0, 0, 0, 0] = two
+    qp = np.zeros((1, 1, 1, 64), dtype=np.uint16)
+    cache = np.zeros((1, 64, 576), dtype=np.uint16)
+    cache[0, 0, 1] = one  # token 0: c_kv = e_1
+    cache[0, 1, 0] = one  # token 1: c_kv = e_0
+    out, lse = mla_decode_ref(qn, qp, cache, np.zeros((1, 1), np.int32), np.array([2], np.int32), 1, 1.0)
+    assert abs(out[0, 0, 0, 0] - g["out0"]) < 1e-15
+    assert abs(out[0, 0, 0, 1] - g["out1"]) < 1e-15
+    assert abs(lse[0, 0, 0] - g["lse"]) < 1e-15
+    assert np.all(out[0, 0, 0, 2:] == 0)
+
+
+# ------------------------------------------------------------ split / merge
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_split_pieces_merge_to_unsplit(q_len):
+    rng = np.random.default_rng(21)
+    wl = W.custom([257, 64, 130, 1000], num_heads=4, q_len=q_len, seed=9)
+    cuts = []
+    for L in wl.seq_lens:
+        L = int(L)
+        k = int(rng.integers(0, min(6, L)))
+        inner = sorted(set(rng.integers(1, L, size=k).tolist())) if L > 1 else []
+        cuts.append([0] + inner + [L])
+    cuts[0] = [0, 256, 257]  # a last piece holding one key only: row 0 of q_len=2 sees nothing there
+    a = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, q_len, wl.scale)
+    b = mla_decode_ref_pieces(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, q_len, wl.scale, cuts)
+    np.testing.assert_allclose(b[0], a[0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(b[1], a[1], rtol=0, atol=1e-12)
+
+
+def test_lse_merge_of_empty_piece_is_neutral():
+    o = np.random.default_rng(1).standard_normal((2, 3, 512))
+    l = np.array([[0.5, -1.0, 2.0], [-np.inf, -np.inf, -np.inf]])
+    out, lse = lse_merge(o, l)
+    np.testing.assert_array_equal(out, o[0])
+    np.testing.assert_array_equal(lse, l[0])
+
+
+# -------------------------------------------------------------- brute force
+def _brute(qn, qp, cache, table, seq_lens, q_len, scale, kv_scale, kv_dtype):
+    """Scalar loops, own gather, math.fsum, softmax without max subtraction."""
+    dec = (lambda r: oracle.bf16_bits_to_f64(r)) if kv_dtype == "bf16" else \
+        (lambda r: oracle.e4m3_to_f64(r) * kv_scale)
+    B, Q, H, _ = qn.shape
+    res = {}
+    for b in range(B):
+        L = int(seq_lens[b])
+        keys = []
+        for t in range(L):
+            page = int(table[b][t // 64])
+            keys.append(list(dec(cache[page, t % 64])))
+        for i in range(Q):
+            n = L - Q + i + 1
+            for h in range(H):
+                q = list(oracle.bf16_bits_to_f64(qn[b, i, h])) + list(oracle.bf16_bits_to_f64(qp[b, i, h]))
+                s = [scale * math.fsum(q[d] * keys[t][d] for d in range(576)) for t in range(n)]
+                e = [math.exp(x) for x in s]
+                z = math.fsum(e)
+                o = [math.fsum(e[t] * keys[t][d] for t in range(n)) / z for d in range(512)]
+                res[(b, i, h)] = (o, math.log(z))
+    return res
+
+
+@pytest.mark.parametrize("q_len,kv_dtype", [(1, "bf16"), (2, "bf16"), (2, "fp8_e4m3")])
+def test_brute_force_tiny(q_len, kv_dtype):
+    wl = W.custom([5, 3], num_heads=2, q_len=q_len, seed=31, kv_dtype=kv_dtype)
+    out, lse = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, q_len, wl.scale,
+                              wl.kv_scale, kv_dtype)
+    ref = _brute(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, q_len, wl.scale, wl.kv_scale, kv_dtype)
+    for (b, i, h), (o, l) in ref.items():
+        np.testing.assert_allclose(out[b, i, h], o, rtol=1e-12, atol=1e-13)
+        assert abs(lse[b, i, h] - l) < 1e-12
+
+
+def test_fp8_path_equals_torch_decoded_values():
+    torch = pytest.importorskip("torch")
+    wl = W.custom([200, 77], num_heads=3, q_len=2, seed=41, kv_dtype="fp8_e4m3")
+    out, lse = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, wl.scale,
+                              wl.kv_scale, "fp8_e4m3")
+    for b in range(2):
+        L = int(wl.seq_lens[b])
+        raw = oracle.gather_rows(wl.kv_cache, wl.page_table[b], L)
+        rows = torch.from_numpy(raw).view(torch.float8_e4m3fn).to(torch.float64).numpy() * wl.kv_scale
+        q = np.concatenate([oracle.bf16_bits_to_f64(wl.q_nope[b]), oracle.bf16_bits_to_f64(wl.q_pe[b])], -1)
+        o, l = attend(q.reshape(-1, 576), rows, np.repeat([L - 1, L], 3), wl.scale)
+        np.testing.assert_array_equal(o.reshape(2, 3, 512), out[b])
+        np.testing.assert_array_equal(l.reshape(2, 3), lse[b])
+
+
+# ------------------------------------------------------------------ causal
+def test_causal_rows_equal_single_position_calls():
+    wl = W.custom([300, 65, 2], num_heads=3, q_len=2, seed=12)
+    out2, lse2 = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, wl.scale)
+    for i, shift in ((1, 0), (0, 1)):
+        qn = np.ascontiguousarray(wl.q_nope[:, i : i + 1])
+        qp = np.ascontiguousarray(wl.q_pe[:, i : i + 1])
+        o1, l1 = mla_decode_ref(qn, qp, wl.kv_cache, wl.page_table, wl.seq_lens - shift, 1, wl.scale)
+        np.testing.assert_allclose(out2[:, i], o1[:, 0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse2[:, i], l1[:, 0], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ invariances
+def test_page_relabelling_is_invisible():
+    wl = W.custom([100, 257, 64], num_heads=2, seed=13)
+    wl2 = W.relabel_pages(wl, seed=99)
+    assert not np.array_equal(wl.page_table, wl2.page_table)
+    a = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 1, wl.scale)
+    b = mla_decode_ref(wl2.q_nope, wl2.q_pe, wl2.kv_cache, wl2.page_table, wl2.seq_lens, 1, wl2.scale)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_prefix_share_equals_prefix_copy():
+    wl = W.prefix_shaped(batch=3, num_heads=2, prefix_pages=3, suffix_range=(10, 100), seed=14)
+    wc = W.copy_shared_prefix(wl)
+    assert wc.num_pages == wl.num_pages + 2 * 3
+    a = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 1, wl.scale)
+    b = mla_decode_ref(wc.q_nope, wc.q_pe, wc.kv_cache, wc.page_table, wc.seq_lens, 1, wc.scale)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_tail_sentinels_do_not_leak(kv_dtype):
+    res = []
+    for sentinel in ("nan", "big", "zero"):
+        wl = W.custom([100, 1, 63], num_heads=2, q_len=1, seed=15, kv_dtype=kv_dtype, sentinel=sentinel)
+        res.append(mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 1, wl.scale,
+                                  wl.kv_scale, kv_dtype))
+    for r in res[1:]:
+        np.testing.assert_array_equal(r[0], res[0][0])
+        np.testing.assert_array_equal(r[1], res[0][1])
+    assert np.all(np.isfinite(res[0][0]))
+
+
+# ----------------------------------------------------------------- errors
+def test_bad_page_id_and_length_are_errors():
+    wl = W.custom([100], num_heads=1, seed=16)
+    bad = wl.page_table.copy()
+    bad[0, 1] = wl.num_pages
+    with pytest.raises(IndexError):
+        mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, bad, wl.seq_lens, 1, wl.scale)
+    with pytest.raises(ValueError):
+        mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, np.array([64 * wl.max_pages + 1]), 1,
+                       wl.scale)
+    with pytest.raises(ValueError):
+        mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, np.array([0]), 1, wl.scale)
+
+
+# ------------------------------------------------------------- workloads
+def test_named_workload_shapes_small():
+    wl = W.make_config("tiny")
+    assert wl.batch == 2 and wl.num_heads == 16 and wl.num_pages == 16
+    assert list(wl.seq_lens) == [100, 257]
+    used = set(wl.page_table[0, :2]) | set(wl.page_table[1, :5])
+    assert len(used) == 7 and all(0 <= p < 16 for p in used)
+    assert abs(wl.scale - 1 / math.sqrt(192)) < 1e-15
