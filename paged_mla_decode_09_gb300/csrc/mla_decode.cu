@@ -1,0 +1,361 @@
+// Host side of the paged MLA decode C ABI (see include/mla_decode.h):
+// argument checks, workspace layout, TMA tensor maps and the three launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mla_decode.h"
+#include "mla_kernels.cuh"
+
+namespace {
+
+using mla::Cfg;
+using mla::Params;
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace: [status words | page prefix sums | cluster slices | fp32
+// partial outputs | partial log-sum-exps].  Sized by B, the cluster count
+// and the number of row blocks only.
+struct Layout {
+  size_t status, prefix, cinfo, o_part, lse_part, total;
+};
+
+Layout workspace_layout(int B, int C, int G) {
+  Layout l;
+  l.status = 0;
+  l.prefix = 256;
+  l.cinfo = l.prefix + align256(static_cast<size_t>(B + 1) * 4);
+  l.o_part = l.cinfo + align256(static_cast<size_t>(C) * 3 * 4);
+  l.lse_part = l.o_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * mla::kDL * 4);
+  l.total = l.lse_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * 4);
+  return l;
+}
+
+int check_dims(const mla_dims* d) {
+  if (!d) return MLA_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->num_heads < 1 || d->q_len < 1 || d->num_pages < 1 || d->max_pages_per_req < 1 ||
+      d->page_table_stride < d->max_pages_per_req)
+    return MLA_ERR_INVALID_ARG;
+  if (d->page_size != 64) return MLA_ERR_UNSUPPORTED;
+  if (d->kv_dtype != MLA_KV_BF16 && d->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->num_heads) * d->q_len > 256) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->num_pages) * 64 > (1ll << 31) - 1) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+int device_ok(int device) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (major != 10 || minor != 3) return MLA_ERR_DEVICE;  // built for sm_103a only
+  return MLA_OK;
+}
+
+// Clusters of 2*G CTAs (one S/O pair per row block) that fit at once.
+struct ShapeCache {
+  std::mutex mu;
+  int clusters[64][2][3] = {};  // [device][fp8][G]
+};
+ShapeCache g_shapes;
+
+int launch_shape(int device, bool f8, int G, int* clusters_out) {
+  if (device < 0 || device >= 64 || G < 1 || G > 2) return MLA_ERR_INVALID_ARG;
+  {
+    std::lock_guard<std::mutex> lk(g_shapes.mu);
+    if (g_shapes.clusters[device][f8][G]) {
+      *clusters_out = g_shapes.clusters[device][f8][G];
+      return MLA_OK;
+    }
+  }
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return MLA_ERR_CUDA;
+  int rc = device_ok(device);
+  int n = 0;
+  if (rc == MLA_OK) {
+    const void* fn = f8 ? reinterpret_cast<const void*>(&mla::mla_decode_kernel<true>)
+                        : reinterpret_cast<const void*>(&mla::mla_decode_kernel<false>);
+    const int smem = f8 ? Cfg<true>::kSmem : Cfg<false>::kSmem;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+      rc = MLA_ERR_CUDA;
+    } else {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * G * 64, 1, 1);
+      cfg.blockDim = dim3(mla::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2 * G;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) rc = MLA_ERR_CUDA;
+    }
+  }
+  if (prev != device) cudaSetDevice(prev);
+  if (rc != MLA_OK) {
+    cudaGetLastError();
+    return rc;
+  }
+  std::lock_guard<std::mutex> lk(g_shapes.mu);
+  g_shapes.clusters[device][f8][G] = n;
+  *clusters_out = n;
+  return MLA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tensor maps over the cache viewed as [num_pages*64 rows][576]: 64-row
+// boxes, 128-byte swizzle (bf16: 64 values; e4m3: 128 values per box row);
+// the e4m3 k_pe part (64 bytes per row) uses a second map with 64-byte swizzle.
+int make_maps(const void* kv, int num_pages, bool f8, CUtensorMap* tm_kv, CUtensorMap* tm_pe) {
+  auto enc = encode_fn();
+  if (!enc) return MLA_ERR_CUDA;
+  const cuuint64_t esz = f8 ? 1 : 2;
+  cuuint64_t gdim[2] = {576, static_cast<cuuint64_t>(num_pages) * 64};
+  cuuint64_t gstr[1] = {576 * esz};
+  cuuint32_t estr[2] = {1, 1};
+  cuuint32_t box[2] = {f8 ? 128u : 64u, 64u};
+  CUresult r = enc(tm_kv, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(kv), gdim, gstr, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+  if (f8) {
+    cuuint32_t box2[2] = {64u, 64u};
+    r = enc(tm_pe, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), gdim, gstr, box2, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+  } else {
+    *tm_pe = *tm_kv;
+  }
+  return MLA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+                const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
+                void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream_v,
+                void* const* events) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (q_len != d->q_len) return MLA_ERR_INVALID_ARG;
+  if (!q_nope || !q_pe || !kv_cache || !page_table || !seq_lens || !out || !lse || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+    return MLA_ERR_ALIGNMENT;
+  int dev = 0;
+  if ((rc = current_device(&dev)) != MLA_OK) return rc;
+  if ((rc = device_ok(dev)) != MLA_OK) return rc;
+  const bool f8 = d->kv_dtype == MLA_KV_FP8_E4M3;
+  const int R = d->num_heads * d->q_len;
+  const int G = (R + mla::kRows - 1) / mla::kRows;
+  int C = 0;
+  if ((rc = launch_shape(dev, f8, G, &C)) != MLA_OK) return rc;
+  const Layout lay = workspace_layout(d->batch, C, G);
+  if (workspace_bytes < lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap tm_kv, tm_pe;
+  if ((rc = make_maps(kv_cache, d->num_pages, f8, &tm_kv, &tm_pe)) != MLA_OK) return rc;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Params p;
+  p.q_nope = static_cast<const uint8_t*>(q_nope);
+  p.q_pe = static_cast<const uint8_t*>(q_pe);
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<uint8_t*>(out);
+  p.lse = lse;
+  p.o_part = reinterpret_cast<float*>(ws + lay.o_part);
+  p.lse_part = reinterpret_cast<float*>(ws + lay.lse_part);
+  p.status = reinterpret_cast<int32_t*>(ws + lay.status);
+  p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
+  p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
+  p.B = d->batch;
+  p.H = d->num_heads;
+  p.Q = d->q_len;
+  p.R = R;
+  p.G = G;
+  p.C = C;
+  p.num_pages = d->num_pages;
+  p.max_pages = d->max_pages_per_req;
+  p.pt_stride = d->page_table_stride;
+  p.scale = scale;
+  p.kv_scale = f8 ? kv_scale : 1.f;
+  p.timeout_ns = kTimeoutNs;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  auto mark = [&](int k) {
+    return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[k]), stream) == cudaSuccess;
+  };
+  if (cudaMemsetAsync(p.status, 0, 16, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (!mark(0)) return MLA_ERR_CUDA;
+  mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  if (!mark(1)) return MLA_ERR_CUDA;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * G * C, 1, 1);
+  cfg.blockDim = dim3(mla::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = f8 ? Cfg<true>::kSmem : Cfg<false>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2 * G;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, tm_kv, tm_pe)
+                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, tm_kv, tm_pe);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (!mark(2)) return MLA_ERR_CUDA;
+  mla::mla_combine_kernel<<<dim3(d->batch, G, mla::kRows / 8), 256, 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  if (!mark(3)) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_ALIGNMENT: return "pointer alignment";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_DEVICE: return "device is not sm_103a";
+    default: return "unknown status";
+  }
+}
+
+int mla_decode_launch_shape(const mla_dims* d, int device, int32_t* clusters, int32_t* cluster_size) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!clusters || !cluster_size) return MLA_ERR_INVALID_ARG;
+  const int G = (d->num_heads * d->q_len + mla::kRows - 1) / mla::kRows;
+  int n = 0;
+  rc = launch_shape(device, d->kv_dtype == MLA_KV_FP8_E4M3, G, &n);
+  if (rc != MLA_OK) return rc;
+  *clusters = n;
+  *cluster_size = 2 * G;
+  return MLA_OK;
+}
+
+size_t mla_decode_workspace_size(const mla_dims* d, int device) {
+  if (check_dims(d) != MLA_OK) return 0;
+  const int G = (d->num_heads * d->q_len + mla::kRows - 1) / mla::kRows;
+  int C = 0;
+  if (launch_shape(device, d->kv_dtype == MLA_KV_FP8_E4M3, G, &C) != MLA_OK) return 0;
+  return workspace_layout(d->batch, C, G).total;
+}
+
+int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+               const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
+               void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, workspace,
+                     workspace_bytes, stream, nullptr);
+}
+
+int mla_decode_profiled(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+                        const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale,
+                        float kv_scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
+                        void* const* events) {
+  if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return MLA_ERR_INVALID_ARG;
+  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, workspace,
+                     workspace_bytes, stream, events);
+}
+
+int mla_query_status(const void* workspace, void* stream_v, int32_t* device_status) {
+  if (!workspace || !device_status) return MLA_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  if (cudaMemcpyAsync(device_status, workspace, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+int mla_gather_rows(const mla_dims* d, const void* kv_cache, const int32_t* page_table, const int32_t* seq_lens,
+                    const int64_t* row_offsets, void* rows_out, void* workspace, void* stream_v) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!kv_cache || !page_table || !seq_lens || !row_offsets || !rows_out || !workspace) return MLA_ERR_INVALID_ARG;
+  if (!aligned(kv_cache, 16) || !aligned(rows_out, 16) || !aligned(workspace, 256) || !aligned(row_offsets, 8))
+    return MLA_ERR_ALIGNMENT;
+  int dev = 0;
+  if ((rc = current_device(&dev)) != MLA_OK) return rc;
+  if ((rc = device_ok(dev)) != MLA_OK) return rc;
+  const bool f8 = d->kv_dtype == MLA_KV_FP8_E4M3;
+  CUtensorMap tm_kv, tm_pe;
+  if ((rc = make_maps(kv_cache, d->num_pages, f8, &tm_kv, &tm_pe)) != MLA_OK) return rc;
+  mla::GatherParams gp;
+  gp.page_table = page_table;
+  gp.seq_lens = seq_lens;
+  gp.row_offsets = row_offsets;
+  gp.rows_out = static_cast<uint8_t*>(rows_out);
+  gp.status = static_cast<int32_t*>(workspace);
+  gp.B = d->batch;
+  gp.num_pages = d->num_pages;
+  gp.max_pages = d->max_pages_per_req;
+  gp.pt_stride = d->page_table_stride;
+  gp.timeout_ns = kTimeoutNs;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const int smem = 64 + 1024 + (f8 ? Cfg<true>::kSlotS : Cfg<false>::kSlotS);
+  if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  cudaError_t e;
+  dim3 grid(d->max_pages_per_req, d->batch);
+  if (f8) {
+    e = cudaFuncSetAttribute(mla::mla_gather_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) mla::mla_gather_kernel<true><<<grid, 128, smem, stream>>>(gp, tm_kv, tm_pe);
+  } else {
+    e = cudaFuncSetAttribute(mla::mla_gather_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) mla::mla_gather_kernel<false><<<grid, 128, smem, stream>>>(gp, tm_kv, tm_pe);
+  }
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream_v) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  if (timeout_us == 0 || timeout_us > 10000000u) return MLA_ERR_INVALID_ARG;
+  int dev = 0, rc;
+  if ((rc = current_device(&dev)) != MLA_OK) return rc;
+  if ((rc = device_ok(dev)) != MLA_OK) return rc;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  mla::mla_wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<int32_t*>(workspace),
+                                                      static_cast<uint64_t>(timeout_us) * 1000ull);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,973 @@
+// Device code of the paged MLA decode: constants, shared-memory layout,
+// schedule (K0), split-KV attention (K1), log-sum-exp combine (K2), the TMA
+// gather test hook and the bounded-wait self-test.
+//
+// Method: TokenSpeed code audit (mlqm.cn/news/403565), 完整技术清单 > MLA —
+// one latent row per token serving as key (576) and value (512), two-stage
+// split-KV decode with fp32 partials merged by log-sum-exp.  Tiling and the
+// online softmax follow the FlashAttention article of the guijiagi.com
+// "推理优化" tag page (same result as plain attention).
+//
+// GB300 design (one row block = up to 128 query rows = heads x drafts):
+//   * a thread-block cluster holds one CTA PAIR per row block;
+//   * the S CTA keeps the row block's absorbed queries in TMEM and computes
+//     S = Q K^T per 64-token page with tcgen05 (A from TMEM, B = the page,
+//     K-major), then the online softmax (one thread per row) and writes the
+//     probabilities P straight into the O CTA's shared memory (DSMEM);
+//   * the O CTA keeps the 128 x 512 fp32 output accumulator in TMEM (all
+//     512 columns) and computes O += P V with V = the same page read through
+//     an MN-major descriptor, applying lazy output rescales;
+//   * pages arrive by TMA (128-byte swizzled boxes of 64 tokens) through the
+//     page table; shared prefix pages are just the same ids, read in place;
+//   * the cluster walks a contiguous, page-balanced slice of all requests'
+//     pages; requests cut by a slice boundary write fp32 partials that the
+//     combine kernel merges by log-sum-exp.
+//
+// Every barrier below is used so that its completer can never run two phases
+// ahead of a waiter (parity waits would then miss a phase).  Where a chain
+// of barriers does not already guarantee that, the barrier is split per
+// P slot (p_full, p_empty, resc_done).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "mla_decode.h"
+#include "sm100_ptx.cuh"
+
+namespace mla {
+
+constexpr int kPage = 64;
+constexpr int kDL = 512;
+constexpr int kDR = 64;
+constexpr int kRows = 128;     // rows per row block = M of every MMA
+constexpr int kThreads = 256;  // 8 warps: 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle, 4-7 row warps
+constexpr int kNS = 3;         // S accumulators in TMEM (S CTA)
+constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..287)
+constexpr int kCtrlBytes = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
+constexpr float kMinusBig = -1.0e30f;      // running-max sentinel (finite, so exp2 never sees inf - inf)
+
+template <bool kF8>
+struct Cfg {
+  static constexpr int kEsz = kF8 ? 1 : 2;
+  static constexpr int kBox = 8192;                     // one TMA box: 64 tokens x 128 bytes
+  static constexpr int kNBoxLat = kF8 ? 4 : 8;          // boxes holding c_kv
+  static constexpr int kPeBytes = kF8 ? 4096 : 8192;    // box holding k_pe
+  static constexpr int kSlotS = kNBoxLat * kBox + kPeBytes;
+  static constexpr int kSlotO = kNBoxLat * kBox;
+  static constexpr int kNStS = kF8 ? 6 : 3;
+  static constexpr int kNStO = kF8 ? 6 : 3;
+  static constexpr int kPBytes = kRows * kPage * kEsz;  // one P tile
+  static constexpr int kPRow = kPage * kEsz;            // bytes of one P row (128 or 64)
+  static constexpr int kKStepsPe = kF8 ? 2 : 4;         // 32-byte K steps in the k_pe box
+  static constexpr uint32_t kPeSwz = kF8 ? kSwizzle64B : kSwizzle128B;
+  static constexpr uint32_t kPeSbo = kF8 ? 512 : 1024;
+  static constexpr uint32_t kPSwz = kF8 ? kSwizzle64B : kSwizzle128B;
+  static constexpr uint32_t kPSbo = kF8 ? 512 : 1024;
+  static constexpr int kPvKSteps = kF8 ? 2 : 4;         // K = 64 tokens in steps of 32 (e4m3) / 16 (bf16)
+  static constexpr int kVKStepBytes = kF8 ? 4096 : 2048;
+  static constexpr int kVBoxesHalf = kF8 ? 2 : 4;       // boxes covering 256 output columns
+  static constexpr uint32_t kIdescQK = make_idesc(kF8, 128, 64, false, false);
+  static constexpr uint32_t kIdescPV = make_idesc(kF8, 128, 256, false, true);
+  static constexpr int kAlphaOff = kNStS * kSlotS;      // S CTA: alpha[2][128] f32
+  static constexpr int kMlOff = kAlphaOff + 2 * kRows * 4;  // S CTA: (m, l)[128]
+  static constexpr int kDataS = kMlOff + 2 * kRows * 4;
+  static constexpr int kPOff = kNStO * kSlotO;          // O CTA: P[2]
+  static constexpr int kDataO = kPOff + 2 * kPBytes;
+  static constexpr int kData = kDataS > kDataO ? kDataS : kDataO;
+  static constexpr int kSmem = kCtrlBytes + 1024 + kData;
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+struct __align__(8) Ctrl {
+  uint64_t kv_full[6];
+  uint64_t kv_empty[6];
+  uint64_t s_full[kNS];
+  uint64_t s_empty[kNS];
+  uint64_t q_full;
+  uint64_t p_full[2];
+  uint64_t p_empty[2];
+  uint64_t o_full;
+  uint64_t o_empty;
+  uint64_t resc_done[2];
+  uint64_t ml_full;
+  uint64_t ml_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int flag[2][4];
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+
+struct Params {
+  const uint8_t* q_nope;   // bf16
+  const uint8_t* q_pe;     // bf16
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  uint8_t* out;            // bf16
+  float* lse;
+  float* o_part;           // [2C][G][128][512]
+  float* lse_part;         // [2C][G][128]
+  int32_t* status;         // [4]: status bits, timeout diagnostics
+  int32_t* prefix;         // [B+1] page prefix sums
+  int32_t* cinfo;          // [C][3] = slice start, slice end, first request
+  int32_t B, H, Q, R, G, C;
+  int32_t num_pages, max_pages, pt_stride;
+  float scale, kv_scale;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ int clamp_len(int L, int max_pages) {
+  return L < 0 ? 0 : (L > max_pages * kPage ? max_pages * kPage : L);
+}
+
+// ---------------------------------------------------------------- K0
+// Page prefix sums over requests and each cluster's page slice
+// [T*c/C, T*(c+1)/C) with the request holding its first page.
+__global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < p.B; base += 1024) {
+    const int b = base + tid;
+    int np = 0;
+    if (b < p.B) {
+      const int L = p.seq_lens[b];
+      if (L < p.Q || L > p.max_pages * kPage) atomicOr(p.status, MLA_DEV_BAD_SEQ_LEN);
+      np = (clamp_len(L, p.max_pages) + kPage - 1) / kPage;
+    }
+    int v = np;  // block-wide inclusive scan
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if ((tid & 31) >= o) v += t;
+    }
+    if ((tid & 31) == 31) warp_tot[tid >> 5] = v;
+    __syncthreads();
+    if (tid < 32) {
+      int w = warp_tot[tid];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, w, o);
+        if (tid >= o) w += t;
+      }
+      warp_tot[tid] = w;
+    }
+    __syncthreads();
+    const int incl = v + ((tid >> 5) ? warp_tot[(tid >> 5) - 1] : 0) + carry;
+    if (b < p.B) p.prefix[b + 1] = incl;
+    __syncthreads();
+    if (tid == 1023) carry = incl;
+    __syncthreads();
+  }
+  if (tid == 0) p.prefix[0] = 0;
+  __syncthreads();
+  const int64_t T = p.prefix[p.B];
+  for (int c = tid; c < p.C; c += 1024) {
+    const int s = static_cast<int>(T * c / p.C);
+    const int e = static_cast<int>(T * (c + 1) / p.C);
+    int lo = 0, hi = p.B - 1;  // last request b with prefix[b] <= s
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.prefix[mid] <= s) lo = mid; else hi = mid - 1;
+    }
+    p.cinfo[3 * c + 0] = s;
+    p.cinfo[3 * c + 1] = e;
+    p.cinfo[3 * c + 2] = lo;
+  }
+}
+
+// One request's piece inside a cluster's slice.
+struct Unit {
+  int b, p0, p1, np, L, slot;  // slot < 0: the piece is the whole request
+};
+
+struct UnitIter {
+  const int32_t* prefix;
+  const int32_t* seq_lens;
+  int B, s, e, b, bfirst, cid, max_pages;
+  __device__ void init(const Params& p, int c) {
+    prefix = p.prefix;
+    seq_lens = p.seq_lens;
+    B = p.B;
+    max_pages = p.max_pages;
+    cid = c;
+    s = p.cinfo[3 * c + 0];
+    e = p.cinfo[3 * c + 1];
+    bfirst = p.cinfo[3 * c + 2];
+    b = bfirst;
+  }
+  __device__ bool next(Unit& u) {
+    while (b < B && s < e) {
+      const int pb0 = prefix[b];
+      if (pb0 >= e) return false;
+      const int pb1 = prefix[b + 1];
+      const int p0 = (s > pb0 ? s : pb0) - pb0;
+      const int p1 = (e < pb1 ? e : pb1) - pb0;
+      const int bb = b++;
+      if (p1 > p0) {
+        u.b = bb;
+        u.p0 = p0;
+        u.p1 = p1;
+        u.np = pb1 - pb0;
+        u.L = clamp_len(seq_lens[bb], max_pages);
+        u.slot = (p0 > 0 || p1 < u.np) ? 2 * cid + (bb != bfirst ? 1 : 0) : -1;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+// Which wait gave up, recorded (first one only) in status[1..3] of the
+// workspace: wait tag, page counter, (cluster << 16) | (rank << 8) | warp.
+enum WaitTag : int {
+  kWaitProdEmptyS = 1, kWaitProdEmptyO, kWaitQFull, kWaitKvFullS, kWaitSEmpty, kWaitSFull, kWaitPEmptyS,
+  kWaitMlEmpty, kWaitKvFullO, kWaitPFullO, kWaitOEmpty, kWaitRescDone, kWaitPFullCorr, kWaitPvPrev,
+  kWaitOFull, kWaitMlFull
+};
+
+__device__ __forceinline__ void raise_timeout(const Params& p, Ctrl* ctrl, uint32_t partner_rank, int tag,
+                                              uint32_t j) {
+  if (atomicCAS(p.status + 1, 0, tag) == 0) {
+    p.status[2] = static_cast<int32_t>(j);
+    p.status[3] = static_cast<int32_t>((cluster_id_x() << 16) | (cluster_ctarank() << 8) | (threadIdx.x >> 5));
+  }
+  atomicOr(p.status, MLA_DEV_TIMEOUT);
+  *reinterpret_cast<volatile int*>(&ctrl->abort) = 1;
+  st_cluster_u32(mapa(smem_u32(&ctrl->abort), partner_rank), 1u);
+}
+
+__device__ __forceinline__ int32_t read_page_id(const Params& p, int b, int pg) {
+  const int32_t pid = __ldg(p.page_table + static_cast<int64_t>(b) * p.pt_stride + pg);
+  if (pid < 0 || pid >= p.num_pages) {
+    atomicOr(p.status, MLA_DEV_BAD_PAGE_ID);
+    return 0;
+  }
+  return pid;
+}
+
+// TMA producer shared by both roles: streams the slice's pages into a ring.
+template <bool kF8, bool kRoleS>
+__device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const CUtensorMap* tm_kv,
+                             const CUtensorMap* tm_pe, int cid, uint32_t partner) {
+  using C = Cfg<kF8>;
+  constexpr int kNSt = kRoleS ? C::kNStS : C::kNStO;
+  constexpr int kSlot = kRoleS ? C::kSlotS : C::kSlotO;
+  volatile int* abort = &ctrl->abort;
+  UnitIter it;
+  it.init(p, cid);
+  Unit u;
+  uint32_t j = 0;
+  bool ok = true;
+  while (ok && it.next(u)) {
+    for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+      const int st = j % kNSt;
+      const uint32_t ph = (j / kNSt) & 1;
+      if (!mbar_wait(smem_u32(&ctrl->kv_empty[st]), ph ^ 1, abort, p.timeout_ns)) {
+        raise_timeout(p, ctrl, partner, kRoleS ? kWaitProdEmptyS : kWaitProdEmptyO, j);
+        ok = false;
+        break;
+      }
+      const int32_t pid = read_page_id(p, u.b, pg);
+      const uint32_t bar = smem_u32(&ctrl->kv_full[st]);
+      uint8_t* slot = ring + st * kSlot;
+      mbar_expect_tx(bar, kSlot);
+      const int y = pid * kPage;
+      for (int d = 0; d < C::kNBoxLat; ++d)
+        tma_load_2d(smem_u32(slot + d * C::kBox), tm_kv, d * (kF8 ? 128 : 64), y, bar);
+      if constexpr (kRoleS) {
+        if constexpr (kF8) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_pe, kDL, y, bar);
+        else tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_kv, kDL, y, bar);
+      }
+    }
+  }
+  // Drain: every load issued into each stage must have landed before exit.
+  const uint32_t issued = j;
+  for (int st = 0; st < kNSt; ++st) {
+    if (static_cast<uint32_t>(st) >= issued) break;
+    const uint32_t last = issued - 1 - ((issued - 1 - st) % kNSt);  // last index with this stage
+    const uint32_t ph = (last / kNSt) & 1;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(&ctrl->kv_full[st]), ph) && globaltimer_ns() - t0 < p.timeout_ns) {
+    }
+  }
+}
+
+// Writes one row's final (unsplit) or partial (split) result.
+template <bool kF8>
+__device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g, int r, uint32_t taddr_row,
+                                          float m_log2, float l) {
+  const int rr = g * kRows + r;
+  const bool real = rr < p.R;
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  const float oscale = kF8 ? p.kv_scale * inv_l : inv_l;
+  const float lse_v = l > 0.f ? (m_log2 + __log2f(l)) * kLn2 : -INFINITY;
+  if (u.slot >= 2 * p.C || u.b >= p.B) {  // cannot happen; checked so a bad schedule never writes out of range
+    atomicOr(p.status, MLA_DEV_INTERNAL);
+    return;
+  }
+  if (u.slot < 0) {
+    const int i = rr / p.H, h = rr % p.H;
+    const int64_t orow = (static_cast<int64_t>(u.b) * p.Q + i) * p.H + h;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDL * 2);
+    for (int c = 0; c < kDL; c += 16) {
+      uint32_t v[16];
+      tmem_ld16(taddr_row + c, v);
+      tmem_wait_ld_tie(v);
+      if (real) {
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * k]) * oscale,
+                                                    __uint_as_float(v[2 * k + 1]) * oscale);
+          w[k] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    if (real) p.lse[orow] = lse_v;
+  } else {
+    const int64_t prow = (static_cast<int64_t>(u.slot) * p.G + g) * kRows + r;
+    float4* dst = reinterpret_cast<float4*>(p.o_part + prow * kDL);
+    for (int c = 0; c < kDL; c += 16) {
+      uint32_t v[16];
+      tmem_ld16(taddr_row + c, v);
+      tmem_wait_ld_tie(v);
+      if (real) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          dst[c / 4 + k] = make_float4(__uint_as_float(v[4 * k]) * oscale, __uint_as_float(v[4 * k + 1]) * oscale,
+                                       __uint_as_float(v[4 * k + 2]) * oscale, __uint_as_float(v[4 * k + 3]) * oscale);
+      }
+    }
+    if (real) p.lse_part[prow] = lse_v;
+  }
+}
+
+// Loads query row r of row block g for request b into TMEM lane r (packed
+// along K: 2 bf16 or 4 e4m3 per column).  For e4m3 returns the row's
+// quantisation scale (value = code * scale).
+template <bool kF8>
+__device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r, uint32_t taddr_row) {
+  const int rr = g * kRows + r;
+  const bool real = rr < p.R;
+  const uint4* qn = nullptr;
+  const uint4* qp = nullptr;
+  if (real) {
+    const int i = rr / p.H, h = rr % p.H;
+    const int64_t row = (static_cast<int64_t>(b) * p.Q + i) * p.H + h;
+    qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
+    qp = reinterpret_cast<const uint4*>(p.q_pe + row * kDR * 2);
+  }
+  // chunk c of 8 bf16 values (16 bytes), c in [0, 72)
+  auto chunk = [&](int c) -> uint4 {
+    if (!real) return make_uint4(0, 0, 0, 0);
+    return c < 64 ? __ldg(qn + c) : __ldg(qp + (c - 64));
+  };
+  if constexpr (!kF8) {
+    for (int c = 0; c < 72; c += 4) {
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = chunk(c + k);
+        w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+      }
+      tmem_st16(taddr_row + c * 4, w);
+    }
+    tmem_wait_st();
+    return 1.f;
+  } else {
+    float amax = 0.f;
+    for (int c = 0; c < 72; ++c) {
+      const uint4 v = chunk(c);
+      const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+    const float qs = amax > 0.f ? amax / 448.f : 1.f;
+    const float inv = 1.f / qs;
+    for (int c = 0; c < 72; c += 8) {  // 64 values -> 16 columns
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = chunk(c + k);
+        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[2 * h2]));
+          const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[2 * h2 + 1]));
+          const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0.x * inv, f0.y * inv), __NV_SATFINITE, __NV_E4M3);
+          const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f1.x * inv, f1.y * inv), __NV_SATFINITE, __NV_E4M3);
+          w[2 * k + h2] = (lo & 0xFFFFu) | (hi << 16);
+        }
+      }
+      tmem_st16(taddr_row + c * 2, w);
+    }
+    tmem_wait_st();
+    return qs;
+  }
+}
+
+// ---------------------------------------------------------------- K1
+template <bool kF8>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_kv,
+                      const __grid_constant__ CUtensorMap tm_pe) {
+  using C = Cfg<kF8>;
+  extern __shared__ uint8_t smem_raw[];
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem_raw);
+  uint8_t* data = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kCtrlBytes + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t rank = cluster_ctarank();
+  const bool role_s = (rank & 1) == 0;
+  const int g = static_cast<int>(rank >> 1);
+  const uint32_t partner = rank ^ 1u;
+  const int cid = static_cast<int>(cluster_id_x());
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 6; ++i) {
+      mbar_init(smem_u32(&ctrl->kv_full[i]), 1);
+      mbar_init(smem_u32(&ctrl->kv_empty[i]), 1);
+    }
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(smem_u32(&ctrl->s_full[i]), 1);
+      mbar_init(smem_u32(&ctrl->s_empty[i]), 128);
+    }
+    mbar_init(smem_u32(&ctrl->q_full), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctrl->p_full[i]), 128);
+      mbar_init(smem_u32(&ctrl->p_empty[i]), 1);
+      mbar_init(smem_u32(&ctrl->resc_done[i]), 128);
+      ctrl->flag[i][0] = ctrl->flag[i][1] = ctrl->flag[i][2] = ctrl->flag[i][3] = 0;
+    }
+    mbar_init(smem_u32(&ctrl->o_full), 1);
+    mbar_init(smem_u32(&ctrl->o_empty), 128);
+    mbar_init(smem_u32(&ctrl->ml_full), 128);
+    mbar_init(smem_u32(&ctrl->ml_empty), 128);
+    mbar_init(smem_u32(&ctrl->drain), 1);
+    ctrl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_kv);
+    if constexpr (kF8) tma_prefetch_desc(&tm_pe);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&ctrl->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // partner barriers initialised before any remote arrive
+  const uint32_t tmem = ctrl->tmem_base;
+  volatile int* abort = &ctrl->abort;
+
+  if (role_s) {
+    // =========================== S CTA ===========================
+    uint8_t* ring = data;
+    float* alpha_buf = reinterpret_cast<float*>(data + C::kAlphaOff);
+    float* ml_buf = reinterpret_cast<float*>(data + C::kMlOff);
+    if (warp == 0) {
+      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_kv, &tm_pe, cid, partner);
+    } else if (warp == 1) {
+      if (lane == 0) {
+        UnitIter it;
+        it.init(p, cid);
+        Unit u;
+        uint32_t j = 0, un = 0;
+        bool ok = true;
+        int why = 0;
+        while (ok && it.next(u)) {
+          if (!mbar_wait(smem_u32(&ctrl->q_full), un & 1, abort, p.timeout_ns)) { ok = false; why = kWaitQFull; break; }
+          for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+            const int st = j % C::kNStS;
+            const int sb = j % kNS;
+            if (!mbar_wait(smem_u32(&ctrl->kv_full[st]), (j / C::kNStS) & 1, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitKvFullS;
+              break;
+            }
+            if (!mbar_wait(smem_u32(&ctrl->s_empty[sb]), ((j / kNS) & 1) ^ 1, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitSEmpty;
+              break;
+            }
+            tc_fence_after();
+            const uint8_t* slot = ring + st * C::kSlotS;
+            const uint32_t dcol = tmem + kSCol0 + sb * 64;
+            uint32_t acc = 0;
+            for (int d = 0; d < C::kNBoxLat; ++d) {
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t bd = smem_desc(smem_u32(slot + d * C::kBox + k * 32), 16, 1024, kSwizzle128B);
+                mma_ts<kF8>(dcol, tmem + d * 32 + k * 8, bd, C::kIdescQK, acc);
+                acc = 1;
+              }
+            }
+            for (int k = 0; k < C::kKStepsPe; ++k) {
+              const uint64_t bd =
+                  smem_desc(smem_u32(slot + C::kNBoxLat * C::kBox + k * 32), 16, C::kPeSbo, C::kPeSwz);
+              mma_ts<kF8>(dcol, tmem + C::kNBoxLat * 32 + k * 8, bd, C::kIdescQK, 1);
+            }
+            mma_commit(smem_u32(&ctrl->kv_empty[st]));
+            mma_commit(smem_u32(&ctrl->s_full[sb]));
+          }
+          ++un;
+        }
+        if (!ok) raise_timeout(p, ctrl, partner, why, j);
+        mma_commit(smem_u32(&ctrl->drain));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&ctrl->drain), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+        }
+      }
+    } else if (warp >= 4) {
+      // ---- softmax: thread r owns query row r of the block
+      const int r = threadIdx.x - 128;
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t p_remote = mapa(smem_u32(data + C::kPOff), partner);
+      const uint32_t pfull_remote0 = mapa(smem_u32(&ctrl->p_full[0]), partner);
+      const uint32_t pfull_remote1 = mapa(smem_u32(&ctrl->p_full[1]), partner);
+      const uint32_t flag_remote = mapa(smem_u32(&ctrl->flag[0][0]), partner);
+      const uint32_t mlfull_remote = mapa(smem_u32(&ctrl->ml_full), partner);
+      const int rr = g * kRows + r;
+      const int qi = rr < p.R ? rr / p.H : p.Q - 1;
+      UnitIter it;
+      it.init(p, cid);
+      Unit u;
+      uint32_t j = 0, un = 0;
+      bool ok = true;
+      int why = 0;
+      while (ok && it.next(u)) {
+        const float qs = load_q_row<kF8>(p, u.b, g, r, tmem + lane_base);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctrl->q_full));
+        const float c2 = p.scale * kLog2e * (kF8 ? qs * p.kv_scale : 1.f);
+        const int nvis = u.L - p.Q + qi + 1;
+        float m_ref = kMinusBig, l = 0.f;
+        for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+          const int sb = j % kNS;
+          if (!mbar_wait_warp(smem_u32(&ctrl->s_full[sb]), (j / kNS) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitSFull;
+            break;
+          }
+          tc_fence_after();
+          uint32_t v[4][16];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tmem + lane_base + kSCol0 + sb * 64 + q4 * 16, v[q4]);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld_tie(v[q4]);
+          tc_fence_before();
+          mbar_arrive(smem_u32(&ctrl->s_empty[sb]));
+          const int t0 = pg * kPage;
+          float x[64];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int t = 0; t < 64; ++t) {
+            const float s = __uint_as_float(v[t >> 4][t & 15]) * c2;
+            x[t] = (t0 + t < nvis) ? s : -INFINITY;  // select: NaN scores of unused slots never pass
+            mx = fmaxf(mx, x[t]);
+          }
+          const bool first = pg == u.p0;
+          float alpha = 1.f;
+          bool resc = false;
+          if (mx > m_ref + kRescaleThreshold) {
+            alpha = ex2_approx(m_ref - mx);
+            m_ref = mx;
+            resc = !first;
+          }
+          const int pb = j & 1;
+          float sum = 0.f;
+          uint32_t pw[kF8 ? 16 : 32];
+          if constexpr (!kF8) {
+#pragma unroll
+            for (int t = 0; t < 64; t += 2) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2_approx(x[t] - m_ref), ex2_approx(x[t + 1] - m_ref));
+              const float2 f = __bfloat1622float2(b2);
+              sum += f.x + f.y;
+              pw[t / 2] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < 64; t += 4) {
+              const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                  make_float2(ex2_approx(x[t] - m_ref), ex2_approx(x[t + 1] - m_ref)), __NV_SATFINITE, __NV_E4M3);
+              const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                  make_float2(ex2_approx(x[t + 2] - m_ref), ex2_approx(x[t + 3] - m_ref)), __NV_SATFINITE, __NV_E4M3);
+              const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
+              const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+              const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&hl));
+              const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hh));
+              sum += (fl.x + fl.y) + (fh.x + fh.y);
+              pw[t / 4] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+          }
+          l = l * alpha + sum;
+          // P slot pb is free once the O CTA finished PV of page j-2
+          if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[pb]), ((j >> 1) & 1) ^ 1, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitPEmptyS;
+            break;
+          }
+          alpha_buf[pb * kRows + r] = alpha;
+          const uint32_t any = __any_sync(0xffffffffu, resc) ? 1u : 0u;
+          if (lane == 0) st_cluster_u32(flag_remote + (pb * 4 + (warp & 3)) * 4, any);
+          const uint32_t prow = p_remote + pb * C::kPBytes + r * C::kPRow;
+          if constexpr (!kF8) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              st_cluster_v4(prow + ((c ^ (r & 7)) << 4),
+                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              st_cluster_v4(prow + ((c ^ ((r >> 1) & 3)) << 4),
+                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]));
+          }
+          fence_proxy_async_cluster();
+          mbar_arrive_cluster(pb ? pfull_remote1 : pfull_remote0);
+        }
+        if (!ok) break;
+        // hand the row's (running max, sum) to the O CTA for the epilogue
+        if (!mbar_wait_warp(smem_u32(&ctrl->ml_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
+          ok = false;
+          why = kWaitMlEmpty;
+          break;
+        }
+        ml_buf[2 * r] = m_ref;
+        ml_buf[2 * r + 1] = l;
+        mbar_arrive_cluster(mlfull_remote);
+        ++un;
+      }
+      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
+    }
+  } else {
+    // =========================== O CTA ===========================
+    uint8_t* ring = data;
+    uint8_t* pbuf = data + C::kPOff;
+    if (warp == 0) {
+      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_kv, &tm_pe, cid, partner);
+    } else if (warp == 1) {
+      UnitIter it;
+      it.init(p, cid);
+      Unit u;
+      uint32_t j = 0, un = 0;
+      bool ok = true;
+      int why = 0;
+      const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << partner));
+      while (ok && it.next(u)) {
+        for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+          const int st = j % C::kNStO;
+          const int pb = j & 1;
+          uint8_t* slot = ring + st * C::kSlotO;
+          if (!mbar_wait_warp(smem_u32(&ctrl->kv_full[st]), (j / C::kNStO) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitKvFullO;
+            break;
+          }
+          const int valid = u.L - pg * kPage;
+          if (valid < kPage) {
+            // slots past the sequence end may hold anything (even NaN): zero
+            // them so that P = 0 there cannot turn into 0 * NaN
+            const int v0 = valid > 0 ? valid : 0;
+            const int nrows = kPage - v0;
+            for (int idx = lane; idx < C::kNBoxLat * nrows * 8; idx += 32) {
+              const int chunk = idx & 7;
+              const int rowi = (idx >> 3) % nrows + v0;
+              const int box = (idx >> 3) / nrows;
+              *reinterpret_cast<uint4*>(slot + box * C::kBox + rowi * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_cta();
+            __syncwarp();
+          }
+          if (!mbar_wait_warp(smem_u32(&ctrl->p_full[pb]), (j >> 1) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitPFullO;
+            break;
+          }
+          const bool first = pg == u.p0;
+          if (first && !mbar_wait_warp(smem_u32(&ctrl->o_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitOEmpty;
+            break;
+          }
+          if (!mbar_wait_warp(smem_u32(&ctrl->resc_done[pb]), (j >> 1) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitRescDone;
+            break;
+          }
+          fence_proxy_async_cta();
+          tc_fence_after();
+          if (lane == 0) {
+            const uint8_t* pt = pbuf + pb * C::kPBytes;
+            for (int k = 0; k < C::kPvKSteps; ++k) {
+              const uint64_t ad = smem_desc(smem_u32(pt + k * 32), 16, C::kPSbo, C::kPSwz);
+              const uint32_t acc = (first && k == 0) ? 0u : 1u;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint64_t bd = smem_desc(smem_u32(slot + h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes),
+                                              C::kBox, 1024, kSwizzle128B);
+                mma_ss<kF8>(tmem + h * 256, ad, bd, C::kIdescPV, acc);
+              }
+            }
+            mma_commit(smem_u32(&ctrl->kv_empty[st]));
+            mma_commit_multicast(smem_u32(&ctrl->p_empty[pb]), mask);
+            if (pg == u.p1 - 1) mma_commit(smem_u32(&ctrl->o_full));
+          }
+          __syncwarp();
+        }
+        ++un;
+      }
+      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
+      if (lane == 0) {
+        mma_commit(smem_u32(&ctrl->drain));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&ctrl->drain), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+        }
+      }
+      __syncwarp();
+    } else if (warp >= 4) {
+      // ---- correction (lazy O rescale) + epilogue: thread r owns row r
+      const int r = threadIdx.x - 128;
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t alpha_remote = mapa(smem_u32(data + C::kAlphaOff), partner);
+      const uint32_t ml_remote = mapa(smem_u32(data + C::kMlOff), partner);
+      const uint32_t mlempty_remote = mapa(smem_u32(&ctrl->ml_empty), partner);
+      UnitIter it;
+      it.init(p, cid);
+      Unit u;
+      uint32_t j = 0, un = 0;
+      bool ok = true;
+      int why = 0;
+      while (ok && it.next(u)) {
+        for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+          const int pb = j & 1;
+          if (!mbar_wait_warp(smem_u32(&ctrl->p_full[pb]), (j >> 1) & 1, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitPFullCorr;
+            break;
+          }
+          const volatile int* fl = ctrl->flag[pb];
+          const bool any = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
+          if (pg != u.p0 && any) {
+            // wait until PV of the previous page has landed in O, then rescale
+            const uint32_t jp = j - 1;
+            if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[jp & 1]), (jp >> 1) & 1, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitPvPrev;
+              break;
+            }
+            tc_fence_after();
+            const float a = __uint_as_float(ld_cluster_u32(alpha_remote + (pb * kRows + r) * 4));
+            if (__any_sync(0xffffffffu, a != 1.f)) {
+              for (int c = 0; c < kDL; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem + lane_base + c, v);
+                tmem_wait_ld_tie(v);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * a);
+                tmem_st16(tmem + lane_base + c, v);
+              }
+              tmem_wait_st();
+            }
+          }
+          // acknowledge page j (rescaled or not); PV of page j waits for this
+          tc_fence_before();
+          mbar_arrive(smem_u32(&ctrl->resc_done[pb]));
+        }
+        if (!ok) break;
+        // epilogue for this unit
+        if (!mbar_wait_warp(smem_u32(&ctrl->o_full), un & 1, abort, p.timeout_ns)) {
+          ok = false;
+          why = kWaitOFull;
+          break;
+        }
+        if (!mbar_wait_warp(smem_u32(&ctrl->ml_full), un & 1, abort, p.timeout_ns)) {
+          ok = false;
+          why = kWaitMlFull;
+          break;
+        }
+        tc_fence_after();
+        const float m_log2 = __uint_as_float(ld_cluster_u32(ml_remote + 8 * r));
+        const float l = __uint_as_float(ld_cluster_u32(ml_remote + 8 * r + 4));
+        mbar_arrive_cluster(mlempty_remote);
+        store_row<kF8>(p, u, g, r, tmem + lane_base, m_log2, l);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctrl->o_empty));
+        ++un;
+      }
+      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, 512);
+  cluster_sync();
+}
+
+// ---------------------------------------------------------------- K2
+// Merges the fp32 partials of every request cut by a slice boundary:
+// lse = log sum_s exp(lse_s), out = sum_s exp(lse_s - lse) * out_s.
+__device__ __forceinline__ int slice_of(int64_t x, int64_t T, int C) {
+  return static_cast<int>(((x + 1) * C - 1) / T);
+}
+
+__global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
+  const int b = blockIdx.x, g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.z * 8 + warp;
+  const int rr = g * kRows + r;
+  if (rr >= p.R) return;
+  const int64_t T = p.prefix[p.B];
+  const int pb0 = p.prefix[b], pb1 = p.prefix[b + 1];
+  if (pb1 <= pb0) return;
+  const int clo = slice_of(pb0, T, p.C), chi = slice_of(pb1 - 1, T, p.C);
+  if (clo == chi) return;
+  // slices strictly between clo and chi may be empty (fewer pages than
+  // clusters): an empty slice holds no piece and is skipped
+  float mx = -INFINITY;
+  for (int c = clo; c <= chi; ++c) {
+    if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
+    const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
+    mx = fmaxf(mx, p.lse_part[(static_cast<int64_t>(slot) * p.G + g) * kRows + r]);
+  }
+  const float base = (mx == -INFINITY) ? 0.f : mx;
+  float z = 0.f;
+  for (int c = clo; c <= chi; ++c) {
+    if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
+    const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
+    z += __expf(p.lse_part[(static_cast<int64_t>(slot) * p.G + g) * kRows + r] - base);
+  }
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = clo; c <= chi; ++c) {
+    if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
+    const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
+    const int64_t prow = (static_cast<int64_t>(slot) * p.G + g) * kRows + r;
+    const float w = __expf(p.lse_part[prow] - base) / z;
+    if (w == 0.f) continue;
+    const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * kDL);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = src[lane + 32 * k];
+      acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
+    }
+  }
+  const int i = rr / p.H, h = rr % p.H;
+  const int64_t orow = (static_cast<int64_t>(b) * p.Q + i) * p.H + h;
+  uint2* dst = reinterpret_cast<uint2*>(p.out + orow * kDL * 2);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+    dst[lane + 32 * k] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+  if (lane == 0) p.lse[orow] = base + __logf(z);
+}
+
+// ------------------------------------------------------ gather test hook
+struct GatherParams {
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int64_t* row_offsets;
+  uint8_t* rows_out;
+  int32_t* status;
+  int32_t B, num_pages, max_pages, pt_stride;
+  uint64_t timeout_ns;
+};
+
+template <bool kF8>
+__global__ void __launch_bounds__(128) mla_gather_kernel(const __grid_constant__ GatherParams gp,
+                                                         const __grid_constant__ CUtensorMap tm_kv,
+                                                         const __grid_constant__ CUtensorMap tm_pe) {
+  using C = Cfg<kF8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
+  int* abort_flag = reinterpret_cast<int*>(smem_raw + 8);
+  uint8_t* page = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 64 + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int pg = blockIdx.x, b = blockIdx.y;
+  const int L = clamp_len(gp.seq_lens[b], gp.max_pages);
+  const int np = (L + kPage - 1) / kPage;
+  if (pg >= np) return;
+  int32_t pid = gp.page_table[static_cast<int64_t>(b) * gp.pt_stride + pg];
+  if (pid < 0 || pid >= gp.num_pages) {
+    if (threadIdx.x == 0) atomicOr(gp.status, MLA_DEV_BAD_PAGE_ID);
+    pid = 0;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(bar), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(smem_u32(bar), C::kSlotS);
+    for (int d = 0; d < C::kNBoxLat; ++d)
+      tma_load_2d(smem_u32(page + d * C::kBox), &tm_kv, d * (kF8 ? 128 : 64), pid * kPage, smem_u32(bar));
+    if constexpr (kF8) tma_load_2d(smem_u32(page + C::kNBoxLat * C::kBox), &tm_pe, kDL, pid * kPage, smem_u32(bar));
+    else tma_load_2d(smem_u32(page + C::kNBoxLat * C::kBox), &tm_kv, kDL, pid * kPage, smem_u32(bar));
+  }
+  if (!mbar_wait(smem_u32(bar), 0, abort_flag, gp.timeout_ns)) {
+    if (threadIdx.x == 0) atomicOr(gp.status, MLA_DEV_TIMEOUT);
+    // the copy may still be in flight: wait for it (bounded) before leaving
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(bar), 0) && globaltimer_ns() - t0 < gp.timeout_ns) {
+    }
+    return;
+  }
+  const int valid = L - pg * kPage < kPage ? L - pg * kPage : kPage;
+  const int row_bytes = 576 * C::kEsz;
+  uint8_t* dst0 = gp.rows_out + (gp.row_offsets[b] + static_cast<int64_t>(pg) * kPage) * row_bytes;
+  // 16-byte chunks: c_kv boxes have 8 chunks per token row, the k_pe box 8 (bf16) or 4 (e4m3)
+  const int lat_chunks = C::kNBoxLat * 8;
+  const int pe_chunks = kF8 ? 4 : 8;
+  const int per_row = lat_chunks + pe_chunks;
+  for (int idx = threadIdx.x; idx < valid * per_row; idx += blockDim.x) {
+    const int t = idx / per_row, c = idx % per_row;
+    uint4 v;
+    if (c < lat_chunks) {
+      const int box = c / 8, ch = c % 8;
+      v = *reinterpret_cast<const uint4*>(page + box * C::kBox + t * 128 + ((ch ^ (t & 7)) << 4));
+    } else {
+      const int ch = c - lat_chunks;
+      if constexpr (kF8)
+        v = *reinterpret_cast<const uint4*>(page + C::kNBoxLat * C::kBox + t * 64 + ((ch ^ ((t >> 1) & 3)) << 4));
+      else
+        v = *reinterpret_cast<const uint4*>(page + C::kNBoxLat * C::kBox + t * 128 + ((ch ^ (t & 7)) << 4));
+    }
+    *reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(t) * row_bytes + c * 16) = v;
+  }
+}
+
+// ---------------------------------------------- bounded-wait self-test
+__global__ void mla_wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // nothing ever arrives on `bar`: the wait must give up after limit_ns
+  if (!mbar_wait(smem_u32(&bar), 0, &abort_flag, limit_ns)) {
+    if (threadIdx.x == 0) atomicOr(status, MLA_DEV_TIMEOUT);
+  }
+}
+
+}  // namespace mla

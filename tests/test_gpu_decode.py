@@ -1,0 +1,225 @@
+"""GPU parity tests: the CUDA path (through the C ABI) against the CPU oracle.
+
+Small cases are compared element by element in full; they span several
+64-token pages, ragged tails, all row-block shapes (H*q_len = 16 ... 256)
+and both cache types.  Invariance tests are bit-exact.
+"""
+import numpy as np
+import pytest
+
+from paged_mla_decode_09_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.build import build_library
+
+    build_library()
+    mla.load_library()
+
+
+from gpu_helpers import TOL, compare, run_gpu  # noqa: E402
+
+
+def test_tiny_config():
+    wl = W.make_config("tiny")
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    print("tiny", compare(wl, out, lse, label="tiny"))
+
+
+RAGGED = [
+    # (seq_lens, H, q_len, dtype)
+    ([1, 2, 63, 64, 65, 127, 128, 129, 500, 1025], 16, 1, "bf16"),
+    ([3000, 70, 64, 1], 64, 1, "bf16"),
+    ([2049, 5000, 33], 128, 1, "bf16"),
+    ([2, 65, 700, 4100], 64, 2, "bf16"),
+    ([1000, 17], 48, 1, "bf16"),
+    ([300, 2500], 100, 2, "bf16"),
+    ([1500, 4100], 16, 2, "fp8_e4m3"),
+    ([2048, 5000, 1100], 128, 2, "fp8_e4m3"),
+    ([5000, 1024], 64, 1, "fp8_e4m3"),
+]
+
+
+@pytest.mark.parametrize("seq_lens,H,Q,dtype", RAGGED)
+def test_ragged_parity(seq_lens, H, Q, dtype):
+    wl = W.custom(seq_lens, num_heads=H, q_len=Q, kv_dtype=dtype, seed=sum(seq_lens) + H)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    print(seq_lens, H, Q, dtype, compare(wl, out, lse, label=f"{seq_lens} H={H} Q={Q} {dtype}"))
+
+
+def test_many_requests_few_pages():
+    """More requests than clusters with short contexts: several requests per
+    cluster slice, most of them unsplit."""
+    rng = np.random.default_rng(3)
+    lens = rng.integers(1, 300, size=300).tolist()
+    wl = W.custom(lens, num_heads=32, q_len=1, seed=5)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    compare(wl, out, lse, label="many-short")
+
+
+def test_long_pipeline_many_pages_per_cluster():
+    """Hundreds of pages per cluster: every pipeline barrier wraps many times
+    and output rescales happen on many pages."""
+    wl = W.custom([20000, 17000, 9000, 12345], num_heads=64, q_len=1, seed=6)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    compare(wl, out, lse, label="long-pipeline")
+
+
+def test_peaked_softmax():
+    """q scaled x4: nearly one-hot weights, where the absolute tolerance term
+    cannot hide errors."""
+    wl = W.custom([700, 3000], num_heads=64, q_len=1, seed=8, q_scale=4.0)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    stats = compare(wl, out, lse, label="peaked")
+    assert stats["max_err_over_rms_ref"] < 0.05, stats
+
+
+def test_single_key_is_bit_exact():
+    wl = W.custom([1, 1, 1], num_heads=64, q_len=1, seed=9)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    import oracle
+
+    for b in range(3):
+        row = oracle.bf16_bits_to_f64(wl.kv_cache[wl.page_table[b, 0], 0, :512])
+        assert np.array_equal(out[b, 0], np.broadcast_to(row, out[b, 0].shape))
+    compare(wl, out, lse, label="single-key")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_tail_sentinels_bit_identical(dtype):
+    outs = []
+    for sentinel in ("nan", "big", "zero"):
+        wl = W.custom([100, 2, 63, 129], num_heads=16, q_len=2, kv_dtype=dtype, seed=15, sentinel=sentinel)
+        out, lse, status, *_ = run_gpu(wl)
+        assert status == 0
+        outs.append((out, lse))
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0])
+        assert np.array_equal(l, outs[0][1])
+
+
+def test_page_relabel_bit_identical():
+    wl = W.custom([100, 1000, 257, 64], num_heads=64, seed=13)
+    wl2 = W.relabel_pages(wl, seed=99)
+    a = run_gpu(wl)
+    b = run_gpu(wl2)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_prefix_share_equals_copy_bit_identical():
+    wl = W.prefix_shaped(batch=6, num_heads=64, prefix_pages=40, suffix_range=(100, 900), seed=14)
+    wc = W.copy_shared_prefix(wl)
+    a = run_gpu(wl)
+    b = run_gpu(wc)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    compare(wl, a[0], a[1], label="prefix-small")
+
+
+def test_causal_rows_match_single_position_calls():
+    wl = W.custom([300, 65, 2, 1000], num_heads=64, q_len=2, seed=12)
+    out2, lse2, st, *_ = run_gpu(wl)
+    assert st == 0
+    atol, rtol = TOL["bf16"]
+    from dataclasses import replace
+
+    for i, shift in ((1, 0), (0, 1)):
+        w1 = replace(wl, q_nope=np.ascontiguousarray(wl.q_nope[:, i:i + 1]),
+                     q_pe=np.ascontiguousarray(wl.q_pe[:, i:i + 1]), q_len=1,
+                     seq_lens=(wl.seq_lens - shift).astype(np.int32))
+        o1, l1, st1, *_ = run_gpu(w1)
+        assert st1 == 0
+        assert np.all(np.abs(out2[:, i] - o1[:, 0]) <= atol + rtol * np.abs(o1[:, 0]))
+        assert np.all(np.abs(lse2[:, i] - l1[:, 0]) <= atol + rtol * np.abs(l1[:, 0]))
+
+
+def test_deterministic_and_cache_untouched():
+    wl = W.custom([5000, 333, 64], num_heads=128, q_len=1, seed=21)
+    a = run_gpu(wl)
+    db = a[3]
+    before = db.kv_cache.view(torch.int16).sum(dtype=torch.int64).item()
+    import paged_mla_decode_09_gb300 as mla
+
+    mla.mla_decode(db.q_nope, db.q_pe, db.kv_cache, db.page_table, db.seq_lens, 1, db.scale, db.kv_scale,
+                   a[4].out, a[4].lse, a[4].workspace)
+    torch.cuda.synchronize()
+    after = db.kv_cache.view(torch.int16).sum(dtype=torch.int64).item()
+    assert before == after
+    assert np.array_equal(a[4].out.float().cpu().numpy().astype(np.float64), a[0])
+
+
+def test_gather_bit_exact():
+    import oracle
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.device_inputs import to_device
+
+    for dtype in ("bf16", "fp8_e4m3"):
+        wl = W.custom([1, 63, 64, 65, 200, 1000], num_heads=1, kv_dtype=dtype, seed=33)
+        db = to_device(wl)
+        offs = np.concatenate([[0], np.cumsum(wl.seq_lens.astype(np.int64))])
+        rows = torch.zeros(int(offs[-1]), 576, dtype=db.kv_cache.dtype, device="cuda")
+        ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+        mla.mla_gather_rows(db.kv_cache, db.page_table, db.seq_lens, torch.from_numpy(offs).cuda(), rows, ws)
+        torch.cuda.synchronize()
+        assert mla.mla_query_status(ws) == 0
+        got = rows.view(torch.int16 if dtype == "bf16" else torch.uint8).cpu().numpy()
+        got = got.view(np.uint16) if dtype == "bf16" else got
+        for b in range(wl.batch):
+            ref = oracle.gather_rows(wl.kv_cache, wl.page_table[b], int(wl.seq_lens[b]))
+            assert np.array_equal(got[offs[b]:offs[b + 1]], ref), (dtype, b)
+
+
+def test_bad_page_id_sets_status_without_fault():
+    import paged_mla_decode_09_gb300 as mla
+
+    wl = W.custom([300, 100], num_heads=16, seed=41)
+    wl.page_table[1, 1] = wl.num_pages + 5
+    out, lse, status, *_ = run_gpu(wl)
+    assert status & mla.MLA_DEV_BAD_PAGE_ID
+    compare(wl, out, lse, requests=[0], label="bad-page other request")  # request 0 is untouched
+
+
+def test_bad_seq_len_sets_status():
+    import paged_mla_decode_09_gb300 as mla
+
+    wl = W.custom([300, 100], num_heads=16, seed=42)
+    wl.seq_lens[1] = 64 * wl.max_pages + 10
+    out, lse, status, *_ = run_gpu(wl)
+    assert status & mla.MLA_DEV_BAD_SEQ_LEN
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    import paged_mla_decode_09_gb300 as mla
+
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    mla.mla_selftest_wait_timeout(ws, 20000)  # 20 ms
+    torch.cuda.synchronize()
+    assert mla.mla_query_status(ws) == mla.MLA_DEV_TIMEOUT
+    wl = W.custom([200], num_heads=16, seed=43)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    compare(wl, out, lse, label="after-timeout")
+
+
+def test_workspace_size_ignores_lengths():
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.device_inputs import to_device
+
+    a = W.custom([64] * 8, num_heads=64, seed=1, extra_cols=200)
+    b = W.custom([64 * 200] * 8, num_heads=64, seed=1)
+    da, dbb = to_device(a), to_device(b)
+    na = mla.mla_decode_workspace_size(mla.make_dims(da.q_nope, da.kv_cache, da.page_table))
+    nb = mla.mla_decode_workspace_size(mla.make_dims(dbb.q_nope, dbb.kv_cache, dbb.page_table))
+    assert na == nb
