@@ -1,0 +1,395 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark for the paged MLA decode library.
+
+One step = one decode of a whole synthetic batch (schedule + split-KV
+attention + log-sum-exp combine) through the C ABI.  Default workload: the
+Kimi-K2-shaped batch (B=64 requests, H=64 heads, q_len=1, 8192 cached tokens
+each, 64-token pages, bf16 latent cache).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+    python bench.py --impl reference ...   # the CPU float64 oracle instead
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun, one rank per GPU)
+every rank decodes its own replica of the batch (requests are independent,
+so the path shards by request with no collective: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_mla_decode_09_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MLA decode KV-tokens/s"
+UNIT = "KV-tokens/s"
+FLOP_PER_ROW_TOKEN = 2 * 576 + 2 * 512  # QK + PV per (query row, visible key)
+L2_FLUSH_BYTES = 512 << 20
+
+
+def algorithmic_work(wl):
+    """Bytes (unique cache rows once + queries + outputs + tables) and FLOPs."""
+    esz = 1 if wl.kv_dtype == "fp8_e4m3" else 2
+    rows_per_page = {}
+    for b in range(wl.batch):
+        L = int(wl.seq_lens[b])
+        for j in range((L + 63) // 64):
+            pid = int(wl.page_table[b, j])
+            rows_per_page[pid] = max(rows_per_page.get(pid, 0), min(64, L - 64 * j))
+    unique_rows = sum(rows_per_page.values())
+    B, Q, H = wl.batch, wl.q_len, wl.num_heads
+    pages_read = sum((int(L) + 63) // 64 for L in wl.seq_lens)
+    nbytes = (unique_rows * 576 * esz + B * Q * H * 576 * 2 + B * Q * H * 512 * 2 + B * Q * H * 4
+              + pages_read * 4 + B * 4)
+    flops = 0
+    for b in range(B):
+        L = int(wl.seq_lens[b])
+        for i in range(Q):
+            flops += (L - Q + i + 1) * H * FLOP_PER_ROW_TOKEN
+    return nbytes, flops, unique_rows
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_rate(wl, budget_s: float, max_requests: int | None = None):
+    """KV-tokens/s of the float64 oracle on a bounded sample of requests."""
+    import oracle
+
+    done_tokens, t_total, reqs = 0, 0.0, []
+    for b in range(wl.batch):
+        t0 = time.perf_counter()
+        oracle.mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len, wl.scale,
+                              wl.kv_scale, wl.kv_dtype, requests=[b])
+        t_total += time.perf_counter() - t0
+        done_tokens += int(wl.seq_lens[b])
+        reqs.append(b)
+        if t_total >= budget_s or (max_requests and len(reqs) >= max_requests):
+            break
+    cores = len(os.sched_getaffinity(0))
+    return done_tokens / t_total, {"requests": len(reqs), "kv_tokens": done_tokens, "seconds": t_total,
+                                   "cores": cores}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    wl = W.make_config(args.config, seed=args.seed)
+    budget = args.ref_step_budget
+    for _ in range(args.warmup):  # untimed warm-up steps
+        cpu_oracle_rate(wl, budget, max_requests=1)
+    rates, secs, samples = [], [], []
+    for _ in range(args.steps):
+        r, info = cpu_oracle_rate(wl, budget)
+        rates.append(r)
+        secs.append(info["seconds"])
+        samples.append(info)
+    value = float(np.mean(rates))
+    sample_desc = (f"{samples[0]['requests']} request(s) of the {args.config} batch per step "
+                   f"({samples[0]['kv_tokens']} KV tokens), float64 numpy oracle")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * float(np.mean(secs)),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.config, **wl.describe()},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": samples[0]["cores"], "kind": "oracle",
+                         "sample": sample_desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.build import build_library
+    from paged_mla_decode_09_gb300.device_inputs import out_to_f64, to_device
+
+    build_library()
+    mla.load_library()
+    wl = W.make_config(args.config, seed=args.seed)
+    db = to_device(wl, dev)
+    bufs = mla.alloc_buffers(db.q_nope, db.kv_cache, db.page_table)
+    nbytes, flops, unique_rows = algorithmic_work(wl)
+    kv_tokens = wl.kv_tokens
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    f8 = wl.kv_dtype == "fp8_e4m3"
+    flop_peak = bf16_peak * (2.0 if f8 else 1.0)  # e4m3 tensor rate = 2x bf16 (nominal ratio)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for evs in ev:  # materialise the event handles
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        mla.mla_decode(db.q_nope, db.q_pe, db.kv_cache, db.page_table, db.seq_lens, db.q_len, db.scale,
+                       db.kv_scale, bufs.out, bufs.lse, bufs.workspace, stream, events=events)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+        torch.cuda.synchronize()
+        status = mla.mla_query_status(bufs.workspace)
+        if status != 0:
+            print(json.dumps({"error": "device status during warm-up", **mla.timeout_diagnostics(bufs.workspace)}),
+                  file=sys.stderr)
+            return 3
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)  # L2 flush between steps (outside the step events)
+            step(ev[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    status = mla.mla_query_status(bufs.workspace)
+    clocks = clk.summary()
+    step_ms = [ev[k][0].elapsed_time(ev[k][3]) for k in range(args.steps)]
+    k1_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    k0_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
+    k2_ms = [ev[k][2].elapsed_time(ev[k][3]) for k in range(args.steps)]
+    ms = float(np.mean(step_ms))
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = kv_tokens * world / (ms * 1e-3)
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs (queries, page table, lengths) from pinned memory, decode, D2H of
+    # out and lse; the cache is resident decode state.
+    h_qn = db.q_nope.cpu().pin_memory()
+    h_qp = db.q_pe.cpu().pin_memory()
+    h_pt = db.page_table.cpu().pin_memory()
+    h_sl = db.seq_lens.cpu().pin_memory()
+    h_out = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+    h_lse = torch.empty(bufs.lse.shape, dtype=bufs.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qp, h_pt, h_sl))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    e2e_ms = []
+    for k in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+        e_start.record(stream)
+        db.q_nope.copy_(h_qn, non_blocking=True)
+        db.q_pe.copy_(h_qp, non_blocking=True)
+        db.page_table.copy_(h_pt, non_blocking=True)
+        db.seq_lens.copy_(h_sl, non_blocking=True)
+        step()
+        h_out.copy_(bufs.out, non_blocking=True)
+        h_lse.copy_(bufs.lse, non_blocking=True)
+        e_end.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e_ms.append(e_start.elapsed_time(e_end))
+    e2e_value = kv_tokens * world / (float(np.mean(e2e_ms)) * 1e-3)
+
+    parity = None  # sampled parity against the oracle on this very batch
+    if rank == 0 and not args.no_parity:
+        import oracle
+
+        reqs = [0, wl.batch - 1]
+        ro, rl = oracle.mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len,
+                                       wl.scale, wl.kv_scale, wl.kv_dtype, requests=reqs)
+        go = out_to_f64(h_out)
+        gl = h_lse.numpy().astype(np.float64)
+        tol = 4e-2 if f8 else 1e-2
+        eo = np.abs(go[reqs] - ro[reqs])
+        el = np.abs(gl[reqs] - rl[reqs])
+        parity = {"requests": reqs, "max_abs_out": float(eo.max()), "max_abs_lse": float(el.max()),
+                  "within_tol": bool(np.all(eo <= tol + tol * np.abs(ro[reqs])) and
+                                     np.all(el <= tol + tol * np.abs(rl[reqs])))}
+
+    k1 = float(np.mean(k1_ms))
+    t_bytes = nbytes / (hbm_peak * 1e9)
+    t_flops = flops / (flop_peak * 1e12)
+    bound = "hbm" if t_bytes >= t_flops else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit_r = nbytes / (k1 * 1e-3) / 1e9, hbm_peak, "GB/s"
+    else:
+        achieved, peak, unit_r = flops / (k1 * 1e-3) / 1e12, flop_peak, "TFLOP/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit_r, "frac": achieved / peak,
+                "traffic": None,
+                "peak_source": peak_src + (" (e4m3 = 2x bf16, nominal ratio)" if f8 and bound == "tensor" else ""),
+                "kernel": "mla_decode_kernel", "alg_bytes": nbytes, "alg_flops": flops,
+                "step_frac": max(t_bytes, t_flops) / (ms * 1e-3)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, info = cpu_oracle_rate(wl, args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+               "sample": f"{info['requests']} request(s), {info['kv_tokens']} KV tokens of the {args.config} "
+                         f"batch, float64 numpy oracle, {info['seconds']:.1f} s"}
+    nclusters, csize = mla.mla_decode_launch_shape(mla.make_dims(db.q_nope, db.kv_cache, db.page_table),
+                                                   dev.index)
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "us_per_step": ms * 1e3,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f8e4m3" if f8 else "bf16",
+            "data": "synthetic",
+            "config": {"workload": args.config, **wl.describe(), "l2": "flushed between steps (512 MiB write)",
+                       "parallelism": f"replicas x{world}", "clusters": nclusters, "cluster_size": csize},
+            "roofline": roofline,
+            "kernel_ms": {"schedule": float(np.mean(k0_ms)), "attention": k1, "combine": float(np.mean(k2_ms))},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+            "device_status": status,
+            "parity_sample": parity,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=list(W.CONFIG_NAMES), default="kimi")
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-step-budget", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
