@@ -49,7 +49,17 @@ constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..2
 constexpr int kCtrlBytes = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
+// Lazy output rescale: O is rescaled only when a row's running max grows by
+// more than the threshold (log2 units).  P is computed relative to the stale
+// max, times 2^shift, so that it never exceeds 2^8 (bf16: threshold 8, no
+// shift).  For e4m3, P is shifted up by 2^5 with threshold 3: the bulk of
+// the probability mass then sits in e4m3's normal range instead of its
+// subnormals; the shift cancels in out = O / l and is removed from the lse.
+template <bool kF8>
+struct SoftmaxCfg {
+  static constexpr float kThreshold = kF8 ? 3.0f : 8.0f;
+  static constexpr float kShift = kF8 ? 5.0f : 0.0f;
+};
 constexpr float kMinusBig = -1.0e30f;      // running-max sentinel (finite, so exp2 never sees inf - inf)
 
 template <bool kF8>
@@ -72,6 +82,11 @@ struct Cfg {
   static constexpr int kPvKSteps = kF8 ? 2 : 4;         // K = 64 tokens in steps of 32 (e4m3) / 16 (bf16)
   static constexpr int kVKStepBytes = kF8 ? 4096 : 2048;
   static constexpr int kVBoxesHalf = kF8 ? 2 : 4;       // boxes covering 256 output columns
+  // e4m3 queries are stored as two terms hi + lo sharing one per-row scale
+  // (hi = e4m3(q/s), lo = e4m3(q/s - hi)); both multiply the same K page and
+  // accumulate into the same S, giving about bf16 precision for q.
+  static constexpr int kQSplit = kF8 ? 2 : 1;
+  static constexpr uint32_t kQLoCol = 144;              // TMEM column of the lo term
   static constexpr uint32_t kIdescQK = make_idesc(kF8, 128, 64, false, false);
   static constexpr uint32_t kIdescPV = make_idesc(kF8, 128, 256, false, true);
   static constexpr int kAlphaOff = kNStS * kSlotS;      // S CTA: alpha[2][128] f32
@@ -307,7 +322,7 @@ __device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g,
   const bool real = rr < p.R;
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
   const float oscale = kF8 ? p.kv_scale * inv_l : inv_l;
-  const float lse_v = l > 0.f ? (m_log2 + __log2f(l)) * kLn2 : -INFINITY;
+  const float lse_v = l > 0.f ? (m_log2 - SoftmaxCfg<kF8>::kShift + __log2f(l)) * kLn2 : -INFINITY;
   if (u.slot >= 2 * p.C || u.b >= p.B) {  // cannot happen; checked so a bad schedule never writes out of range
     atomicOr(p.status, MLA_DEV_INTERNAL);
     return;
@@ -396,8 +411,18 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
     }
     const float qs = amax > 0.f ? amax / 448.f : 1.f;
     const float inv = 1.f / qs;
-    for (int c = 0; c < 72; c += 8) {  // 64 values -> 16 columns
-      uint32_t w[16];
+    // two e4m3 codes for a pair of scaled values: hi = e4m3(x), lo = e4m3(x - hi)
+    auto split2 = [](float2 x, uint32_t& hi16, uint32_t& lo16) {
+      const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      const __nv_fp8x2_storage_t l =
+          __nv_cvt_float2_to_fp8x2(make_float2(x.x - hf.x, x.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+      hi16 = h;
+      lo16 = l;
+    };
+    for (int c = 0; c < 72; c += 8) {  // 64 values -> 16 columns of each term
+      uint32_t whi[16], wlo[16];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint4 v = chunk(c + k);
@@ -406,12 +431,15 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
         for (int h2 = 0; h2 < 2; ++h2) {
           const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[2 * h2]));
           const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[2 * h2 + 1]));
-          const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0.x * inv, f0.y * inv), __NV_SATFINITE, __NV_E4M3);
-          const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f1.x * inv, f1.y * inv), __NV_SATFINITE, __NV_E4M3);
-          w[2 * k + h2] = (lo & 0xFFFFu) | (hi << 16);
+          uint32_t h0, l0, h1, l1;
+          split2(make_float2(f0.x * inv, f0.y * inv), h0, l0);
+          split2(make_float2(f1.x * inv, f1.y * inv), h1, l1);
+          whi[2 * k + h2] = (h0 & 0xFFFFu) | (h1 << 16);
+          wlo[2 * k + h2] = (l0 & 0xFFFFu) | (l1 << 16);
         }
       }
-      tmem_st16(taddr_row + c * 2, w);
+      tmem_st16(taddr_row + c * 2, whi);
+      tmem_st16(taddr_row + Cfg<kF8>::kQLoCol + c * 2, wlo);
     }
     tmem_wait_st();
     return qs;
@@ -508,17 +536,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t* slot = ring + st * C::kSlotS;
             const uint32_t dcol = tmem + kSCol0 + sb * 64;
             uint32_t acc = 0;
-            for (int d = 0; d < C::kNBoxLat; ++d) {
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t bd = smem_desc(smem_u32(slot + d * C::kBox + k * 32), 16, 1024, kSwizzle128B);
-                mma_ts<kF8>(dcol, tmem + d * 32 + k * 8, bd, C::kIdescQK, acc);
-                acc = 1;
+#pragma unroll 1
+            for (int term = 0; term < C::kQSplit; ++term) {
+              const uint32_t qcol = tmem + (term ? C::kQLoCol : 0u);
+              for (int d = 0; d < C::kNBoxLat; ++d) {
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t bd = smem_desc(smem_u32(slot + d * C::kBox + k * 32), 16, 1024, kSwizzle128B);
+                  mma_ts<kF8>(dcol, qcol + d * 32 + k * 8, bd, C::kIdescQK, acc);
+                  acc = 1;
+                }
               }
-            }
-            for (int k = 0; k < C::kKStepsPe; ++k) {
-              const uint64_t bd =
-                  smem_desc(smem_u32(slot + C::kNBoxLat * C::kBox + k * 32), 16, C::kPeSbo, C::kPeSwz);
-              mma_ts<kF8>(dcol, tmem + C::kNBoxLat * 32 + k * 8, bd, C::kIdescQK, 1);
+              for (int k = 0; k < C::kKStepsPe; ++k) {
+                const uint64_t bd =
+                    smem_desc(smem_u32(slot + C::kNBoxLat * C::kBox + k * 32), 16, C::kPeSbo, C::kPeSwz);
+                mma_ts<kF8>(dcol, qcol + C::kNBoxLat * 32 + k * 8, bd, C::kIdescQK, 1);
+              }
             }
             mma_commit(smem_u32(&ctrl->kv_empty[st]));
             mma_commit(smem_u32(&ctrl->s_full[sb]));
@@ -582,18 +614,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool first = pg == u.p0;
           float alpha = 1.f;
           bool resc = false;
-          if (mx > m_ref + kRescaleThreshold) {
+          if (mx > m_ref + SoftmaxCfg<kF8>::kThreshold) {
             alpha = ex2_approx(m_ref - mx);
             m_ref = mx;
             resc = !first;
           }
           const int pb = j & 1;
+          const float m_sh = m_ref - SoftmaxCfg<kF8>::kShift;  // P = 2^(x - m_ref + shift)
           float sum = 0.f;
           uint32_t pw[kF8 ? 16 : 32];
           if constexpr (!kF8) {
 #pragma unroll
             for (int t = 0; t < 64; t += 2) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2_approx(x[t] - m_ref), ex2_approx(x[t + 1] - m_ref));
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2_approx(x[t] - m_sh), ex2_approx(x[t + 1] - m_sh));
               const float2 f = __bfloat1622float2(b2);
               sum += f.x + f.y;
               pw[t / 2] = *reinterpret_cast<uint32_t*>(&b2);
@@ -602,9 +635,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < 64; t += 4) {
               const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                  make_float2(ex2_approx(x[t] - m_ref), ex2_approx(x[t + 1] - m_ref)), __NV_SATFINITE, __NV_E4M3);
+                  make_float2(ex2_approx(x[t] - m_sh), ex2_approx(x[t + 1] - m_sh)), __NV_SATFINITE, __NV_E4M3);
               const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                  make_float2(ex2_approx(x[t + 2] - m_ref), ex2_approx(x[t + 3] - m_ref)), __NV_SATFINITE, __NV_E4M3);
+                  make_float2(ex2_approx(x[t + 2] - m_sh), ex2_approx(x[t + 3] - m_sh)), __NV_SATFINITE, __NV_E4M3);
               const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
               const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
               const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&hl));

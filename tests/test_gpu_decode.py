@@ -45,6 +45,8 @@ RAGGED = [
     ([1500, 4100], 16, 2, "fp8_e4m3"),
     ([2048, 5000, 1100], 128, 2, "fp8_e4m3"),
     ([5000, 1024], 64, 1, "fp8_e4m3"),
+    ([64, 129, 700], 64, 1, "fp8_e4m3"),
+    ([2, 65, 129, 700], 16, 2, "fp8_e4m3"),
 ]
 
 
