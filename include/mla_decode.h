@@ -51,7 +51,8 @@ typedef enum {
   MLA_ERR_ALIGNMENT = -3,        /* a pointer breaks the alignment rule of its argument */
   MLA_ERR_WORKSPACE_TOO_SMALL = -4,
   MLA_ERR_CUDA = -5,             /* a CUDA runtime/driver call failed */
-  MLA_ERR_DEVICE = -6            /* the current device is not sm_103a */
+  MLA_ERR_DEVICE = -6,           /* the current device is not sm_103a */
+  MLA_ERR_SCRATCH_TOO_SMALL = -7 /* mla_decode_noalloc: dimensions need more than its static scratch */
 } mla_status;
 
 /* Device-side status bits (word 0 of the workspace). */
@@ -150,6 +151,31 @@ int mla_gather_rows(const mla_dims* d, const void* kv_cache, const int32_t* page
  * context stays usable.
  */
 int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream);
+
+/*
+ * Allocation-free variant of mla_decode (no counterpart in the pages: it
+ * exists for callers that cannot call cudaMalloc, such as a serving loop
+ * that must not allocate, a process whose device memory is all handed to
+ * its own pool, or a plug-in that only receives buffers from its host).
+ * Same arguments and results as mla_decode, but there is no workspace: the
+ * status words, schedule and split partials live in a static 16 MiB device
+ * array inside this library (every GPU that loads the library holds it
+ * until the process exits).  The caller still passes all inputs and
+ * outputs.  Nothing is allocated or freed.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - The call runs on fewer clusters when the split partials of all the
+ *     device's clusters would not fit in 16 MiB; if even one cluster's do
+ *     not (very large batches), it returns MLA_ERR_SCRATCH_TOO_SMALL.
+ *   - All calls share the one array, which keeps the last call's contents:
+ *     calls that may overlap on the GPU (other streams, other threads)
+ *     race and must be serialised by the caller.
+ *   - status_out (device int32, may be NULL) receives a copy of the device
+ *     status word (MLA_DEV_* bits) at the end of the call, on `stream`.
+ */
+int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+                       const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale,
+                       float kv_scale, void* out, float* lse, int32_t* status_out, void* stream);
 
 /* Static description of a status code. */
 const char* mla_status_string(int status);

@@ -30,6 +30,7 @@ ENTRY_POINTS = (
     "mla_selftest_wait_timeout",
     "mla_status_string",
     "mla_decode_launch_shape",
+    "mla_decode_noalloc",
 )
 
 
@@ -88,6 +89,8 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.mla_status_string.restype = ctypes.c_char_p
     lib.mla_decode_launch_shape.argtypes = [D, ctypes.c_int, ctypes.POINTER(I32), ctypes.POINTER(I32)]
     lib.mla_decode_launch_shape.restype = ctypes.c_int
+    lib.mla_decode_noalloc.argtypes = [D, P, P, P, P, P, I32, ctypes.c_float, ctypes.c_float, P, P, P, P]
+    lib.mla_decode_noalloc.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib

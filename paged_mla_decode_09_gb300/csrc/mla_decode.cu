@@ -254,6 +254,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MLA_ERR_CUDA: return "CUDA error";
     case MLA_ERR_DEVICE: return "device is not sm_103a";
+    case MLA_ERR_SCRATCH_TOO_SMALL: return "dimensions exceed the 16 MiB static scratch of mla_decode_noalloc";
     default: return "unknown status";
   }
 }
@@ -359,3 +360,129 @@ int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Allocation-free decode.  Some callers cannot call cudaMalloc: code that
+// runs where a device allocation is not allowed or not wanted (an inference
+// server that must not allocate in its serving loop, a process that hands
+// every byte of device memory to its own pool up front, plug-ins that only
+// receive buffers from their host).  mla_decode_noalloc serves them by
+// taking its scratch (status words, schedule, split partials) from a static
+// device array that lives in this library's module instead of a
+// caller-provided workspace.  Every GPU that loads the library holds this
+// array until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current (in host code the symbol itself is only a stand-in).
+struct NoAllocScratch {
+  std::mutex mu;
+  void* ptr[64] = {};
+};
+NoAllocScratch g_noalloc;
+
+int noalloc_scratch(int device, uint8_t** out) {
+  if (device < 0 || device >= 64) return MLA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_noalloc.mu);
+  if (!g_noalloc.ptr[device]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    g_noalloc.ptr[device] = ptr;
+  }
+  *out = static_cast<uint8_t*>(g_noalloc.ptr[device]);
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+                                  const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale,
+                                  float kv_scale, void* out, float* lse, int32_t* status_out, void* stream_v) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (q_len != d->q_len) return MLA_ERR_INVALID_ARG;
+  if (!q_nope || !q_pe || !kv_cache || !page_table || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
+      (status_out && !aligned(status_out, 4)))
+    return MLA_ERR_ALIGNMENT;
+  int dev = 0;
+  if ((rc = current_device(&dev)) != MLA_OK) return rc;
+  if ((rc = device_ok(dev)) != MLA_OK) return rc;
+  const bool f8 = d->kv_dtype == MLA_KV_FP8_E4M3;
+  const int R = d->num_heads * d->q_len;
+  const int G = (R + mla::kRows - 1) / mla::kRows;
+  int C = 0;
+  if ((rc = launch_shape(dev, f8, G, &C)) != MLA_OK) return rc;
+  // Fewer clusters than the device could hold when the split partials of all
+  // of them would not fit in the fixed scratch; none at all is an error.
+  while (C > 0 && workspace_layout(d->batch, C, G).total > kNoAllocScratchBytes) --C;
+  if (C < 1) return MLA_ERR_SCRATCH_TOO_SMALL;
+  const Layout lay = workspace_layout(d->batch, C, G);
+  uint8_t* ws = nullptr;
+  if ((rc = noalloc_scratch(dev, &ws)) != MLA_OK) return rc;
+  CUtensorMap tm_kv, tm_pe;
+  if ((rc = make_maps(kv_cache, d->num_pages, f8, &tm_kv, &tm_pe)) != MLA_OK) return rc;
+
+  Params p;
+  p.q_nope = static_cast<const uint8_t*>(q_nope);
+  p.q_pe = static_cast<const uint8_t*>(q_pe);
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<uint8_t*>(out);
+  p.lse = lse;
+  p.o_part = reinterpret_cast<float*>(ws + lay.o_part);
+  p.lse_part = reinterpret_cast<float*>(ws + lay.lse_part);
+  p.status = reinterpret_cast<int32_t*>(ws + lay.status);
+  p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
+  p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
+  p.B = d->batch;
+  p.H = d->num_heads;
+  p.Q = d->q_len;
+  p.R = R;
+  p.G = G;
+  p.C = C;
+  p.num_pages = d->num_pages;
+  p.max_pages = d->max_pages_per_req;
+  p.pt_stride = d->page_table_stride;
+  p.scale = scale;
+  p.kv_scale = f8 ? kv_scale : 1.f;
+  p.timeout_ns = kTimeoutNs;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  // the status words must start at zero; everything else in the scratch is
+  // written before it is read within the call
+  if (cudaMemsetAsync(p.status, 0, 16, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * G * C, 1, 1);
+  cfg.blockDim = dim3(mla::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = f8 ? Cfg<true>::kSmem : Cfg<false>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2 * G;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, tm_kv, tm_pe)
+                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, tm_kv, tm_pe);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  mla::mla_combine_kernel<<<dim3(d->batch, G, mla::kRows / 8), 256, 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  if (status_out &&
+      cudaMemcpyAsync(status_out, p.status, 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
