@@ -486,3 +486,11 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
     return MLA_ERR_CUDA;
   return MLA_OK;
 }
+
+#ifdef MLA_TRACE
+// Trace builds only: copies the event stamps of cluster 0 to host memory.
+extern "C" int mla_trace_copy(void* host_dst, size_t bytes) {
+  if (bytes > sizeof(mla::g_mla_trace)) bytes = sizeof(mla::g_mla_trace);
+  return cudaMemcpyFromSymbol(host_dst, mla::g_mla_trace, bytes) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+#endif

@@ -137,6 +137,20 @@ struct Params {
   uint64_t timeout_ns;
 };
 
+// Optional event trace (built only with -DMLA_TRACE): global-timer stamps
+// of each pipeline event per page for cluster 0, for latency analysis.
+#ifdef MLA_TRACE
+__device__ uint64_t g_mla_trace[2][16][1024];
+#define MLA_TRACE_POINT(role, ev, j)                                                    \
+  do {                                                                                  \
+    if (cluster_id_x() == 0 && (j) < 1024) g_mla_trace[(role)][(ev)][(j)] = globaltimer_ns(); \
+  } while (0)
+#else
+#define MLA_TRACE_POINT(role, ev, j) \
+  do {                               \
+  } while (0)
+#endif
+
 __device__ __forceinline__ int clamp_len(int L, int max_pages) {
   return L < 0 ? 0 : (L > max_pages * kPage ? max_pages * kPage : L);
 }
@@ -300,6 +314,7 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
         if constexpr (kF8) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_pe, kDL, y, bar);
         else tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_kv, kDL, y, bar);
       }
+      MLA_TRACE_POINT(kRoleS ? 0 : 1, 0, j);
     }
   }
   // Drain: every load issued into each stage must have landed before exit.
@@ -532,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               why = kWaitSEmpty;
               break;
             }
+            MLA_TRACE_POINT(0, 1, j);
             tc_fence_after();
             const uint8_t* slot = ring + st * C::kSlotS;
             const uint32_t dcol = tmem + kSCol0 + sb * 64;
@@ -554,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(smem_u32(&ctrl->kv_empty[st]));
             mma_commit(smem_u32(&ctrl->s_full[sb]));
+            MLA_TRACE_POINT(0, 2, j);
           }
           ++un;
         }
@@ -594,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             why = kWaitSFull;
             break;
           }
+          if (r == 0) MLA_TRACE_POINT(0, 3, j);
           tc_fence_after();
           uint32_t v[4][16];
 #pragma unroll
@@ -653,6 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             why = kWaitPEmptyS;
             break;
           }
+          if (r == 0) MLA_TRACE_POINT(0, 4, j);
           alpha_buf[pb * kRows + r] = alpha;
           const uint32_t any = __any_sync(0xffffffffu, resc) ? 1u : 0u;
           if (lane == 0) st_cluster_u32(flag_remote + (pb * 4 + (warp & 3)) * 4, any);
@@ -670,6 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_cluster();
           mbar_arrive_cluster(pb ? pfull_remote1 : pfull_remote0);
+          if (r == 0) MLA_TRACE_POINT(0, 5, j);
         }
         if (!ok) break;
         // hand the row's (running max, sum) to the O CTA for the epilogue
@@ -709,6 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             why = kWaitKvFullO;
             break;
           }
+          if (lane == 0) MLA_TRACE_POINT(1, 1, j);
           const int valid = u.L - pg * kPage;
           if (valid < kPage) {
             // slots past the sequence end may hold anything (even NaN): zero
@@ -729,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             why = kWaitPFullO;
             break;
           }
+          if (lane == 0) MLA_TRACE_POINT(1, 2, j);
           const bool first = pg == u.p0;
           if (first && !mbar_wait_warp(smem_u32(&ctrl->o_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
             ok = false;
@@ -757,6 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&ctrl->kv_empty[st]));
             mma_commit_multicast(smem_u32(&ctrl->p_empty[pb]), mask);
             if (pg == u.p1 - 1) mma_commit(smem_u32(&ctrl->o_full));
+            MLA_TRACE_POINT(1, 3, j);
           }
           __syncwarp();
         }
@@ -791,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             why = kWaitPFullCorr;
             break;
           }
+          if (r == 0) MLA_TRACE_POINT(1, 4, j);
           const volatile int* fl = ctrl->flag[pb];
           const bool any = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
           if (pg != u.p0 && any) {
@@ -818,6 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // acknowledge page j (rescaled or not); PV of page j waits for this
           tc_fence_before();
           mbar_arrive(smem_u32(&ctrl->resc_done[pb]));
+          if (r == 0) MLA_TRACE_POINT(1, 5, j);
         }
         if (!ok) break;
         // epilogue for this unit
@@ -835,7 +860,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_log2 = __uint_as_float(ld_cluster_u32(ml_remote + 8 * r));
         const float l = __uint_as_float(ld_cluster_u32(ml_remote + 8 * r + 4));
         mbar_arrive_cluster(mlempty_remote);
+        if (r == 0) MLA_TRACE_POINT(1, 6, un);
         store_row<kF8>(p, u, g, r, tmem + lane_base, m_log2, l);
+        if (r == 0) MLA_TRACE_POINT(1, 7, un);
         tc_fence_before();
         mbar_arrive(smem_u32(&ctrl->o_empty));
         ++un;
