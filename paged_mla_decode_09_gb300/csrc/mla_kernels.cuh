@@ -46,7 +46,7 @@ constexpr int kRows = 128;     // rows per row block = M of every MMA
 constexpr int kThreads = 256;  // 8 warps: 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle, 4-7 row warps
 constexpr int kNS = 3;         // S accumulators in TMEM (S CTA)
 constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..287)
-constexpr int kCtrlBytes = 1024;
+constexpr int kCtrlBytes = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy output rescale: O is rescaled only when a row's running max grows by
@@ -89,13 +89,16 @@ struct Cfg {
   static constexpr uint32_t kQLoCol = 144;              // TMEM column of the lo term
   static constexpr uint32_t kIdescQK = make_idesc(kF8, 128, 64, false, false);
   static constexpr uint32_t kIdescPV = make_idesc(kF8, 128, 256, false, true);
-  static constexpr int kAlphaOff = kNStS * kSlotS;      // S CTA: alpha[2][128] f32
-  static constexpr int kMlOff = kAlphaOff + 2 * kRows * 4;  // S CTA: (m, l)[128]
+  static constexpr int kMlOff = kNStS * kSlotS;         // S CTA: (m, l)[128]
   static constexpr int kDataS = kMlOff + 2 * kRows * 4;
   static constexpr int kPOff = kNStO * kSlotO;          // O CTA: P[2]
-  static constexpr int kDataO = kPOff + 2 * kPBytes;
+  static constexpr int kAlphaOff = kPOff + 2 * kPBytes; // O CTA: alpha[2][128] f32 (sent with P)
+  static constexpr int kDataO = kAlphaOff + 2 * kRows * 4;
   static constexpr int kData = kDataS > kDataO ? kDataS : kDataO;
-  static constexpr int kSmem = kCtrlBytes + 1024 + kData;
+  // dynamic smem = alignment slack + 1024-aligned data + control block
+  static constexpr int kSmem = 1024 + kData + kCtrlBytes;
+  // bytes the S CTA sends per page: P tile + one alpha per row
+  static constexpr uint32_t kPTx = kPBytes + kRows * 4;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -115,7 +118,6 @@ struct __align__(8) Ctrl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int flag[2][4];
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
@@ -468,9 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_pe) {
   using C = Cfg<kF8>;
   extern __shared__ uint8_t smem_raw[];
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem_raw);
-  uint8_t* data = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + kCtrlBytes + 1023) &
+  uint8_t* data = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(data + C::kData);
   const uint32_t rank = cluster_ctarank();
   const bool role_s = (rank & 1) == 0;
   const int g = static_cast<int>(rank >> 1);
@@ -489,10 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&ctrl->q_full), 128);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&ctrl->p_full[i]), 128);
+      mbar_init(smem_u32(&ctrl->p_full[i]), 1);  // one arm (expect_tx) by the O MMA warp + P bytes
       mbar_init(smem_u32(&ctrl->p_empty[i]), 1);
       mbar_init(smem_u32(&ctrl->resc_done[i]), 128);
-      ctrl->flag[i][0] = ctrl->flag[i][1] = ctrl->flag[i][2] = ctrl->flag[i][3] = 0;
     }
     mbar_init(smem_u32(&ctrl->o_full), 1);
     mbar_init(smem_u32(&ctrl->o_empty), 128);
@@ -520,7 +521,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (role_s) {
     // =========================== S CTA ===========================
     uint8_t* ring = data;
-    float* alpha_buf = reinterpret_cast<float*>(data + C::kAlphaOff);
     float* ml_buf = reinterpret_cast<float*>(data + C::kMlOff);
     if (warp == 0) {
       if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_kv, &tm_pe, cid, partner);
@@ -585,9 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = threadIdx.x - 128;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t p_remote = mapa(smem_u32(data + C::kPOff), partner);
+      const uint32_t alpha_remote = mapa(smem_u32(data + C::kAlphaOff), partner);
       const uint32_t pfull_remote0 = mapa(smem_u32(&ctrl->p_full[0]), partner);
       const uint32_t pfull_remote1 = mapa(smem_u32(&ctrl->p_full[1]), partner);
-      const uint32_t flag_remote = mapa(smem_u32(&ctrl->flag[0][0]), partner);
       const uint32_t mlfull_remote = mapa(smem_u32(&ctrl->ml_full), partner);
       const int rr = g * kRows + r;
       const int qi = rr < p.R ? rr / p.H : p.Q - 1;
@@ -629,13 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             x[t] = (t0 + t < nvis) ? s : -INFINITY;  // select: NaN scores of unused slots never pass
             mx = fmaxf(mx, x[t]);
           }
-          const bool first = pg == u.p0;
+          const bool first = pg == u.p0;  // O is overwritten on a unit's first page
           float alpha = 1.f;
-          bool resc = false;
           if (mx > m_ref + SoftmaxCfg<kF8>::kThreshold) {
-            alpha = ex2_approx(m_ref - mx);
+            alpha = first ? 0.f : ex2_approx(m_ref - mx);
             m_ref = mx;
-            resc = !first;
           }
           const int pb = j & 1;
           const float m_sh = m_ref - SoftmaxCfg<kF8>::kShift;  // P = 2^(x - m_ref + shift)
@@ -672,23 +670,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (r == 0) MLA_TRACE_POINT(0, 4, j);
-          alpha_buf[pb * kRows + r] = alpha;
-          const uint32_t any = __any_sync(0xffffffffu, resc) ? 1u : 0u;
-          if (lane == 0) st_cluster_u32(flag_remote + (pb * 4 + (warp & 3)) * 4, any);
+          // P row (swizzled for the MMA) and alpha go straight into the O
+          // CTA's shared memory; the bytes complete on its p_full barrier
+          const uint32_t bar = pb ? pfull_remote1 : pfull_remote0;
           const uint32_t prow = p_remote + pb * C::kPBytes + r * C::kPRow;
           if constexpr (!kF8) {
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              st_cluster_v4(prow + ((c ^ (r & 7)) << 4),
-                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]));
+              st_async_v4(prow + ((c ^ (r & 7)) << 4),
+                          make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]), bar);
           } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              st_cluster_v4(prow + ((c ^ ((r >> 1) & 3)) << 4),
-                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]));
+              st_async_v4(prow + ((c ^ ((r >> 1) & 3)) << 4),
+                          make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]), bar);
           }
-          fence_proxy_async_cluster();
-          mbar_arrive_cluster(pb ? pfull_remote1 : pfull_remote0);
+          st_async_b32(alpha_remote + (pb * kRows + r) * 4, __float_as_uint(alpha), bar);
           if (r == 0) MLA_TRACE_POINT(0, 5, j);
         }
         if (!ok) break;
@@ -719,6 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int why = 0;
       const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << partner));
+      if (lane == 0) {  // arm the P barriers for pages 0 and 1 (bytes may land before or after)
+        mbar_expect_tx(smem_u32(&ctrl->p_full[0]), C::kPTx);
+        mbar_expect_tx(smem_u32(&ctrl->p_full[1]), C::kPTx);
+      }
       while (ok && it.next(u)) {
         for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
           const int st = j % C::kNStO;
@@ -750,6 +751,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             why = kWaitPFullO;
             break;
           }
+          // phase for page j done: arm this P slot for page j + 2.  Its bytes
+          // cannot come earlier: the S CTA sends them only after PV(j) ended.
+          if (lane == 0) mbar_expect_tx(smem_u32(&ctrl->p_full[pb]), C::kPTx);
           if (lane == 0) MLA_TRACE_POINT(1, 2, j);
           const bool first = pg == u.p0;
           if (first && !mbar_wait_warp(smem_u32(&ctrl->o_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
@@ -797,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- correction (lazy O rescale) + epilogue: thread r owns row r
       const int r = threadIdx.x - 128;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t alpha_remote = mapa(smem_u32(data + C::kAlphaOff), partner);
+      const float* alpha_buf = reinterpret_cast<const float*>(data + C::kAlphaOff);
       const uint32_t ml_remote = mapa(smem_u32(data + C::kMlOff), partner);
       const uint32_t mlempty_remote = mapa(smem_u32(&ctrl->ml_empty), partner);
       UnitIter it;
@@ -815,9 +819,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (r == 0) MLA_TRACE_POINT(1, 4, j);
-          const volatile int* fl = ctrl->flag[pb];
-          const bool any = (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
-          if (pg != u.p0 && any) {
+          const float a = alpha_buf[pb * kRows + r];
+          if (pg != u.p0 && __any_sync(0xffffffffu, a != 1.f)) {
             // wait until PV of the previous page has landed in O, then rescale
             const uint32_t jp = j - 1;
             if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[jp & 1]), (jp >> 1) & 1, abort, p.timeout_ns)) {
@@ -826,8 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const float a = __uint_as_float(ld_cluster_u32(alpha_remote + (pb * kRows + r) * 4));
-            if (__any_sync(0xffffffffu, a != 1.f)) {
+            {
               for (int c = 0; c < kDL; c += 16) {
                 uint32_t v[16];
                 tmem_ld16(tmem + lane_base + c, v);
