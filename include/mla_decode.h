@@ -99,8 +99,8 @@ size_t mla_decode_workspace_size(const mla_dims* d, int device);
  *   seq_lens    int32 [B]; L_b counts the q_len new tokens, already in the
  *               cache; position i sees keys 0 .. L_b - q_len + i
  *   q_len       must equal d->q_len
- *   scale       softmax scale applied to the whole score (e.g. 1/sqrt(192))
- *   kv_scale    per-tensor dequantisation scale of an e4m3 cache (ignored for bf16)
+ *   scale       softmax scale applied to the whole score (e.g. 1/sqrt(192)); > 0
+ *   kv_scale    per-tensor dequantisation scale of an e4m3 cache, > 0 (ignored for bf16)
  *   out         bf16 [B][q_len][H][512], 16-byte aligned
  *   lse         fp32 [B][q_len][H], natural log of sum exp(score)
  *   workspace   >= mla_decode_workspace_size bytes, 256-byte aligned device memory;

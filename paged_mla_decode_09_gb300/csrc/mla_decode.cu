@@ -164,6 +164,9 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   if (q_len != d->q_len) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !kv_cache || !page_table || !seq_lens || !out || !lse || !workspace)
     return MLA_ERR_INVALID_ARG;
+  // the softmax scale (and an e4m3 cache's scale) must be positive and finite
+  if (!(scale > 0.f) || scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
+  if (d->kv_dtype == MLA_KV_FP8_E4M3 && (!(kv_scale > 0.f) || kv_scale > 3.0e38f)) return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
     return MLA_ERR_ALIGNMENT;
@@ -408,6 +411,8 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   if (rc != MLA_OK) return rc;
   if (q_len != d->q_len) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !kv_cache || !page_table || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
+  if (d->kv_dtype == MLA_KV_FP8_E4M3 && (!(kv_scale > 0.f) || kv_scale > 3.0e38f)) return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
       (status_out && !aligned(status_out, 4)))

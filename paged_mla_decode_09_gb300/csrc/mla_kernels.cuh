@@ -549,24 +549,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             MLA_TRACE_POINT(0, 1, j);
             tc_fence_after();
-            const uint8_t* slot = ring + st * C::kSlotS;
+            // descriptors of box 0 / the k_pe box at K step 0; a K step adds
+            // 32 bytes (2 in the >>4 address field), a box adds 8 KB (512)
+            const uint32_t slot_addr = smem_u32(ring + st * C::kSlotS);
+            const uint64_t dlat = smem_desc(slot_addr, 16, 1024, kSwizzle128B);
+            const uint64_t dpe = smem_desc(slot_addr + C::kNBoxLat * C::kBox, 16, C::kPeSbo, C::kPeSwz);
             const uint32_t dcol = tmem + kSCol0 + sb * 64;
-            uint32_t acc = 0;
-#pragma unroll 1
+#pragma unroll
             for (int term = 0; term < C::kQSplit; ++term) {
               const uint32_t qcol = tmem + (term ? C::kQLoCol : 0u);
+#pragma unroll
               for (int d = 0; d < C::kNBoxLat; ++d) {
-                for (int k = 0; k < 4; ++k) {
-                  const uint64_t bd = smem_desc(smem_u32(slot + d * C::kBox + k * 32), 16, 1024, kSwizzle128B);
-                  mma_ts<kF8>(dcol, qcol + d * 32 + k * 8, bd, C::kIdescQK, acc);
-                  acc = 1;
-                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mma_ts<kF8>(dcol, qcol + d * 32 + k * 8, dlat + static_cast<uint64_t>(d * 512 + k * 2),
+                              C::kIdescQK, (term | d | k) ? 1u : 0u);
               }
-              for (int k = 0; k < C::kKStepsPe; ++k) {
-                const uint64_t bd =
-                    smem_desc(smem_u32(slot + C::kNBoxLat * C::kBox + k * 32), 16, C::kPeSbo, C::kPeSwz);
-                mma_ts<kF8>(dcol, qcol + C::kNBoxLat * 32 + k * 8, bd, C::kIdescQK, 1);
-              }
+#pragma unroll
+              for (int k = 0; k < C::kKStepsPe; ++k)
+                mma_ts<kF8>(dcol, qcol + C::kNBoxLat * 32 + k * 8, dpe + static_cast<uint64_t>(k * 2), C::kIdescQK,
+                            1u);
             }
             mma_commit(smem_u32(&ctrl->kv_empty[st]));
             mma_commit(smem_u32(&ctrl->s_full[sb]));
@@ -621,14 +623,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(smem_u32(&ctrl->s_empty[sb]));
           const int t0 = pg * kPage;
-          float x[64];
-          float mx = -INFINITY;
+          // every key of the page visible to this row: no per-key masking
+          const bool full = t0 + kPage <= nvis;
+#define MLA_S(t) __uint_as_float(v[(t) >> 4][(t) & 15])
+          float mxr = -INFINITY;  // max of the raw scores (c2 > 0, so scaling commutes with max)
+          if (full) {
 #pragma unroll
-          for (int t = 0; t < 64; ++t) {
-            const float s = __uint_as_float(v[t >> 4][t & 15]) * c2;
-            x[t] = (t0 + t < nvis) ? s : -INFINITY;  // select: NaN scores of unused slots never pass
-            mx = fmaxf(mx, x[t]);
+            for (int t = 0; t < 64; ++t) mxr = fmaxf(mxr, MLA_S(t));
+          } else {
+#pragma unroll
+            for (int t = 0; t < 64; ++t)
+              if (t0 + t < nvis) mxr = fmaxf(mxr, MLA_S(t));  // unused slots (even NaN) never pass
           }
+          const float mx = mxr * c2;
           const bool first = pg == u.p0;  // O is overwritten on a unit's first page
           float alpha = 1.f;
           if (mx > m_ref + SoftmaxCfg<kF8>::kThreshold) {
@@ -636,24 +643,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_ref = mx;
           }
           const int pb = j & 1;
-          const float m_sh = m_ref - SoftmaxCfg<kF8>::kShift;  // P = 2^(x - m_ref + shift)
+          const float nm = SoftmaxCfg<kF8>::kShift - m_ref;  // P = 2^(s * c2 - m_ref + shift)
           float sum = 0.f;
           uint32_t pw[kF8 ? 16 : 32];
+          auto prob = [&](int t) {
+            const float e = ex2_approx(fmaf(MLA_S(t), c2, nm));
+            return (full || t0 + t < nvis) ? e : 0.f;
+          };
           if constexpr (!kF8) {
 #pragma unroll
             for (int t = 0; t < 64; t += 2) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(ex2_approx(x[t] - m_sh), ex2_approx(x[t + 1] - m_sh));
-              const float2 f = __bfloat1622float2(b2);
-              sum += f.x + f.y;
+              const float a = prob(t), b = prob(t + 1);
+              sum += a + b;  // bf16 rounding of P changes l by < 2^-9 relative
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
               pw[t / 2] = *reinterpret_cast<uint32_t*>(&b2);
             }
           } else {
 #pragma unroll
             for (int t = 0; t < 64; t += 4) {
-              const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                  make_float2(ex2_approx(x[t] - m_sh), ex2_approx(x[t + 1] - m_sh)), __NV_SATFINITE, __NV_E4M3);
-              const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                  make_float2(ex2_approx(x[t + 2] - m_sh), ex2_approx(x[t + 3] - m_sh)), __NV_SATFINITE, __NV_E4M3);
+              const __nv_fp8x2_storage_t lo =
+                  __nv_cvt_float2_to_fp8x2(make_float2(prob(t), prob(t + 1)), __NV_SATFINITE, __NV_E4M3);
+              const __nv_fp8x2_storage_t hi =
+                  __nv_cvt_float2_to_fp8x2(make_float2(prob(t + 2), prob(t + 3)), __NV_SATFINITE, __NV_E4M3);
+              // l sums the e4m3-rounded P actually multiplied into O
               const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
               const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
               const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&hl));
@@ -662,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pw[t / 4] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
             }
           }
+#undef MLA_S
           l = l * alpha + sum;
           // P slot pb is free once the O CTA finished PV of page j-2
           if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[pb]), ((j >> 1) & 1) ^ 1, abort, p.timeout_ns)) {
@@ -769,16 +782,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_cta();
           tc_fence_after();
           if (lane == 0) {
-            const uint8_t* pt = pbuf + pb * C::kPBytes;
+            const uint64_t dp = smem_desc(smem_u32(pbuf + pb * C::kPBytes), 16, C::kPSbo, C::kPSwz);
+            const uint64_t dv = smem_desc(smem_u32(slot), C::kBox, 1024, kSwizzle128B);
+#pragma unroll
             for (int k = 0; k < C::kPvKSteps; ++k) {
-              const uint64_t ad = smem_desc(smem_u32(pt + k * 32), 16, C::kPSbo, C::kPSwz);
               const uint32_t acc = (first && k == 0) ? 0u : 1u;
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint64_t bd = smem_desc(smem_u32(slot + h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes),
-                                              C::kBox, 1024, kSwizzle128B);
-                mma_ss<kF8>(tmem + h * 256, ad, bd, C::kIdescPV, acc);
-              }
+              for (int h = 0; h < 2; ++h)
+                mma_ss<kF8>(tmem + h * 256, dp + static_cast<uint64_t>(k * 2),
+                            dv + static_cast<uint64_t>((h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes) >> 4),
+                            C::kIdescPV, acc);
             }
             mma_commit(smem_u32(&ctrl->kv_empty[st]));
             mma_commit_multicast(smem_u32(&ctrl->p_empty[pb]), mask);

@@ -99,6 +99,14 @@ def test_null_and_misaligned_pointers(lib):
     assert lib.mla_decode(ctypes.byref(d), P, P, P, P, P, 1, 1.0, 1.0, P, P, W, 1 << 30, None) == -3
 
 
+@pytest.mark.parametrize("scale,kv_scale,dtype", [(0.0, 1.0, 0), (-1.0, 1.0, 0), (float("nan"), 1.0, 0),
+                                                   (float("inf"), 1.0, 0), (0.1, 0.0, 1), (0.1, float("nan"), 1)])
+def test_scales_must_be_positive_and_finite(lib, scale, kv_scale, dtype):
+    d = _dims(kv_dtype=dtype)
+    assert lib.mla_decode(ctypes.byref(d), P, P, P, P, P, 1, scale, kv_scale, P, P, P, 1 << 30, None) == -1
+    assert lib.mla_decode_noalloc(ctypes.byref(d), P, P, P, P, P, 1, scale, kv_scale, P, P, None, None) == -1
+
+
 def test_profiled_entry_needs_four_events(lib):
     d = _dims()
     ev = (ctypes.c_void_p * 4)(None, None, None, None)
