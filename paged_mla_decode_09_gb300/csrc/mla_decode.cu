@@ -124,29 +124,45 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Tensor maps over the cache viewed as [num_pages*64 rows][576]: 64-row
-// boxes, 128-byte swizzle (bf16: 64 values; e4m3: 128 values per box row);
-// the e4m3 k_pe part (64 bytes per row) uses a second map with 64-byte swizzle.
-int make_maps(const void* kv, int num_pages, bool f8, CUtensorMap* tm_kv, CUtensorMap* tm_pe) {
+// Tensor maps over the cache.  Each page is fetched with one 3-D box whose
+// dimensions are (64 or 128 values of a row, 64 token rows 576 values apart,
+// box index 128 bytes apart): the box lands in shared memory as [box][row]
+// [128 bytes] with 128-byte swizzle, the K-major / MN-major layout the MMAs
+// read.  tm_s: the S CTA's page (bf16: all 9 boxes; e4m3: the 4 c_kv boxes),
+// tm_o: the O CTA's c_kv boxes, tm_pe: the e4m3 k_pe part (64-byte rows,
+// 64-byte swizzle, 2-D).
+struct Maps {
+  CUtensorMap s, o, pe;
+};
+
+int make_maps(const void* kv, int num_pages, bool f8, Maps* m) {
   auto enc = encode_fn();
   if (!enc) return MLA_ERR_CUDA;
-  const cuuint64_t esz = f8 ? 1 : 2;
-  cuuint64_t gdim[2] = {576, static_cast<cuuint64_t>(num_pages) * 64};
-  cuuint64_t gstr[1] = {576 * esz};
-  cuuint32_t estr[2] = {1, 1};
-  cuuint32_t box[2] = {f8 ? 128u : 64u, 64u};
-  CUresult r = enc(tm_kv, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                   const_cast<void*>(kv), gdim, gstr, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const cuuint64_t rows = static_cast<cuuint64_t>(num_pages) * 64;
+  const cuuint64_t row_bytes = f8 ? 576 : 1152;
+  const cuuint32_t box_vals = f8 ? 128 : 64;  // one 128-byte swizzle row
+  cuuint64_t gdim[3] = {box_vals, rows, f8 ? 4u : 9u};
+  cuuint64_t gstr[2] = {row_bytes, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint32_t box_s[3] = {box_vals, 64, f8 ? 4u : 9u};
+  CUresult r = enc(&m->s, dt, 3, const_cast<void*>(kv), gdim, gstr, box_s, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+  cuuint32_t box_o[3] = {box_vals, 64, f8 ? 4u : 8u};
+  r = enc(&m->o, dt, 3, const_cast<void*>(kv), gdim, gstr, box_o, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
   if (f8) {
+    cuuint64_t gdim2[2] = {576, rows};
+    cuuint64_t gstr2[1] = {576};
     cuuint32_t box2[2] = {64u, 64u};
-    r = enc(tm_pe, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), gdim, gstr, box2, estr,
+    r = enc(&m->pe, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), gdim2, gstr2, box2, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
   } else {
-    *tm_pe = *tm_kv;
+    m->pe = m->s;
   }
   return MLA_OK;
 }
@@ -180,8 +196,8 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   if ((rc = launch_shape(dev, f8, G, &C)) != MLA_OK) return rc;
   const Layout lay = workspace_layout(d->batch, C, G);
   if (workspace_bytes < lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  CUtensorMap tm_kv, tm_pe;
-  if ((rc = make_maps(kv_cache, d->num_pages, f8, &tm_kv, &tm_pe)) != MLA_OK) return rc;
+  Maps maps;
+  if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Params p;
@@ -231,8 +247,8 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, tm_kv, tm_pe)
-                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, tm_kv, tm_pe);
+  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe)
+                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
@@ -319,8 +335,8 @@ int mla_gather_rows(const mla_dims* d, const void* kv_cache, const int32_t* page
   if ((rc = current_device(&dev)) != MLA_OK) return rc;
   if ((rc = device_ok(dev)) != MLA_OK) return rc;
   const bool f8 = d->kv_dtype == MLA_KV_FP8_E4M3;
-  CUtensorMap tm_kv, tm_pe;
-  if ((rc = make_maps(kv_cache, d->num_pages, f8, &tm_kv, &tm_pe)) != MLA_OK) return rc;
+  Maps maps;
+  if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
   mla::GatherParams gp;
   gp.page_table = page_table;
   gp.seq_lens = seq_lens;
@@ -339,10 +355,10 @@ int mla_gather_rows(const mla_dims* d, const void* kv_cache, const int32_t* page
   dim3 grid(d->max_pages_per_req, d->batch);
   if (f8) {
     e = cudaFuncSetAttribute(mla::mla_gather_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) mla::mla_gather_kernel<true><<<grid, 128, smem, stream>>>(gp, tm_kv, tm_pe);
+    if (e == cudaSuccess) mla::mla_gather_kernel<true><<<grid, 128, smem, stream>>>(gp, maps.s, maps.pe);
   } else {
     e = cudaFuncSetAttribute(mla::mla_gather_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) mla::mla_gather_kernel<false><<<grid, 128, smem, stream>>>(gp, tm_kv, tm_pe);
+    if (e == cudaSuccess) mla::mla_gather_kernel<false><<<grid, 128, smem, stream>>>(gp, maps.s, maps.pe);
   }
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
@@ -432,8 +448,8 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   const Layout lay = workspace_layout(d->batch, C, G);
   uint8_t* ws = nullptr;
   if ((rc = noalloc_scratch(dev, &ws)) != MLA_OK) return rc;
-  CUtensorMap tm_kv, tm_pe;
-  if ((rc = make_maps(kv_cache, d->num_pages, f8, &tm_kv, &tm_pe)) != MLA_OK) return rc;
+  Maps maps;
+  if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
 
   Params p;
   p.q_nope = static_cast<const uint8_t*>(q_nope);
@@ -478,8 +494,8 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, tm_kv, tm_pe)
-                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, tm_kv, tm_pe);
+  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe)
+                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

@@ -310,12 +310,10 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
       uint8_t* slot = ring + st * kSlot;
       mbar_expect_tx(bar, kSlot);
       const int y = pid * kPage;
-      for (int d = 0; d < C::kNBoxLat; ++d)
-        tma_load_2d(smem_u32(slot + d * C::kBox), tm_kv, d * (kF8 ? 128 : 64), y, bar);
-      if constexpr (kRoleS) {
-        if constexpr (kF8) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_pe, kDL, y, bar);
-        else tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_kv, kDL, y, bar);
-      }
+      // one 3-D box = the whole page (or its c_kv part) in box-major,
+      // 128-byte-swizzled order: per-copy overhead dominates small copies
+      tma_load_3d(smem_u32(slot), tm_kv, 0, y, 0, bar);
+      if constexpr (kRoleS && kF8) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_pe, kDL, y, bar);
       MLA_TRACE_POINT(kRoleS ? 0 : 1, 0, j);
     }
   }
@@ -466,8 +464,8 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
 // ---------------------------------------------------------------- K1
 template <bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_kv,
-                      const __grid_constant__ CUtensorMap tm_pe) {
+    mla_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_s,
+                      const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_pe) {
   using C = Cfg<kF8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* data = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -504,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(role_s ? &tm_s : &tm_o);
     if constexpr (kF8) tma_prefetch_desc(&tm_pe);
   }
   if (warp == 2) {
@@ -523,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = data;
     float* ml_buf = reinterpret_cast<float*>(data + C::kMlOff);
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_kv, &tm_pe, cid, partner);
+      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, cid, partner);
     } else if (warp == 1) {
       if (lane == 0) {
         UnitIter it;
@@ -720,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = data;
     uint8_t* pbuf = data + C::kPOff;
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_kv, &tm_pe, cid, partner);
+      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, cid, partner);
     } else if (warp == 1) {
       UnitIter it;
       it.init(p, cid);
@@ -967,7 +965,7 @@ struct GatherParams {
 
 template <bool kF8>
 __global__ void __launch_bounds__(128) mla_gather_kernel(const __grid_constant__ GatherParams gp,
-                                                         const __grid_constant__ CUtensorMap tm_kv,
+                                                         const __grid_constant__ CUtensorMap tm_s,
                                                          const __grid_constant__ CUtensorMap tm_pe) {
   using C = Cfg<kF8>;
   extern __shared__ uint8_t smem_raw[];
@@ -991,11 +989,10 @@ __global__ void __launch_bounds__(128) mla_gather_kernel(const __grid_constant__
   }
   __syncthreads();
   if (threadIdx.x == 0) {
+    // exactly the loads of the decode kernel's S CTA
     mbar_expect_tx(smem_u32(bar), C::kSlotS);
-    for (int d = 0; d < C::kNBoxLat; ++d)
-      tma_load_2d(smem_u32(page + d * C::kBox), &tm_kv, d * (kF8 ? 128 : 64), pid * kPage, smem_u32(bar));
+    tma_load_3d(smem_u32(page), &tm_s, 0, pid * kPage, 0, smem_u32(bar));
     if constexpr (kF8) tma_load_2d(smem_u32(page + C::kNBoxLat * C::kBox), &tm_pe, kDL, pid * kPage, smem_u32(bar));
-    else tma_load_2d(smem_u32(page + C::kNBoxLat * C::kBox), &tm_kv, kDL, pid * kPage, smem_u32(bar));
   }
   if (!mbar_wait(smem_u32(bar), 0, abort_flag, gp.timeout_ns)) {
     if (threadIdx.x == 0) atomicOr(gp.status, MLA_DEV_TIMEOUT);
