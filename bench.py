@@ -155,6 +155,30 @@ def dist_setup():
     return world, rank, local
 
 
+def rank_seed(base_seed, config: str, rank: int):
+    """Seed of rank `rank`'s replica: rank 0 decodes the standard batch, the
+    others independent batches of the same shape."""
+    if base_seed is None:
+        base_seed = W.default_seed(config)
+    return base_seed + 7919 * rank
+
+
+def reduce_over_ranks(ms: float, kv_tokens: int, device):
+    """Whole-job figures of a replicated step: the slowest rank's time and
+    the KV tokens all ranks decoded.  Every rank must call it (a collective
+    when the process group is up); with one process it is the identity."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms, kv_tokens
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([kv_tokens], dtype=torch.int64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -214,7 +238,7 @@ def run_ours(args):
 
     build_library()
     mla.load_library()
-    wl = W.make_config(args.config, seed=args.seed)
+    wl = W.make_config(args.config, seed=rank_seed(args.seed, args.config, rank))
     db = to_device(wl, dev)
     bufs = mla.alloc_buffers(db.q_nope, db.kv_cache, db.page_table)
     nbytes, flops, unique_rows = algorithmic_work(wl)
@@ -262,12 +286,8 @@ def run_ours(args):
     k1_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
     k0_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     k2_ms = [ev[k][2].elapsed_time(ev[k][3]) for k in range(args.steps)]
-    ms = float(np.mean(step_ms))
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = kv_tokens * world / (ms * 1e-3)
+    ms, job_tokens = reduce_over_ranks(float(np.mean(step_ms)), kv_tokens, dev)
+    value = job_tokens / (ms * 1e-3)
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs (queries, page table, lengths) from pinned memory, decode, D2H of
@@ -298,7 +318,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         if k >= args.warmup:
             e2e_ms.append(e_start.elapsed_time(e_end))
-    e2e_value = kv_tokens * world / (float(np.mean(e2e_ms)) * 1e-3)
+    e2e_max_ms, _ = reduce_over_ranks(float(np.mean(e2e_ms)), kv_tokens, dev)
+    e2e_value = job_tokens / (e2e_max_ms * 1e-3)
 
     parity = None  # sampled parity against the oracle on this very batch
     if rank == 0 and not args.no_parity:

@@ -248,10 +248,14 @@ def custom(
     return build(name, num_heads, q_len, seq_lens, table, pool, rng, seed, kv_dtype, scale, sentinel, q_scale)
 
 
+def default_seed(name: str) -> int:
+    """Seed of a named batch: 1000 + its index in CONFIG_NAMES."""
+    return 1000 + CONFIG_NAMES.index(name)
+
+
 def make_config(name: str, seed: int | None = None, sentinel: str = "nan") -> Workload:
-    """One of the five named decode batches (default seed = 1000 + index)."""
-    idx = CONFIG_NAMES.index(name)
-    seed = 1000 + idx if seed is None else seed
+    """One of the five named decode batches (default seed: default_seed(name))."""
+    seed = default_seed(name) if seed is None else seed
     rng = np.random.Generator(np.random.PCG64(seed))
     if name == "tiny":
         seq_lens = np.array([100, 257], dtype=np.int32)
