@@ -145,11 +145,12 @@ int make_maps(const void* kv, int num_pages, bool f8, Maps* m) {
   cuuint64_t gstr[2] = {row_bytes, 128};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  cuuint32_t box_s[3] = {box_vals, 64, f8 ? 4u : 9u};
+  // one copy = one ring part: kBoxesPartS / kBoxesPartO 128-byte columns of 64 token rows
+  cuuint32_t box_s[3] = {box_vals, 64, static_cast<cuuint32_t>(f8 ? Cfg<true>::kBoxesPartS : Cfg<false>::kBoxesPartS)};
   CUresult r = enc(&m->s, dt, 3, const_cast<void*>(kv), gdim, gstr, box_s, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
-  cuuint32_t box_o[3] = {box_vals, 64, f8 ? 4u : 8u};
+  cuuint32_t box_o[3] = {box_vals, 64, static_cast<cuuint32_t>(f8 ? Cfg<true>::kBoxesPartO : Cfg<false>::kBoxesPartO)};
   r = enc(&m->o, dt, 3, const_cast<void*>(kv), gdim, gstr, box_o, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
@@ -201,6 +202,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Params p;
+  p.kv = static_cast<const uint8_t*>(kv_cache);
   p.q_nope = static_cast<const uint8_t*>(q_nope);
   p.q_pe = static_cast<const uint8_t*>(q_pe);
   p.page_table = page_table;
@@ -452,6 +454,7 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
 
   Params p;
+  p.kv = static_cast<const uint8_t*>(kv_cache);
   p.q_nope = static_cast<const uint8_t*>(q_nope);
   p.q_pe = static_cast<const uint8_t*>(q_pe);
   p.page_table = page_table;

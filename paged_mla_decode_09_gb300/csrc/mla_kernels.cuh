@@ -43,10 +43,18 @@ constexpr int kPage = 64;
 constexpr int kDL = 512;
 constexpr int kDR = 64;
 constexpr int kRows = 128;     // rows per row block = M of every MMA
-constexpr int kThreads = 256;  // 8 warps: 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle, 4-7 row warps
+// 12 warps: 0 TMA, 1 and 3 MMA, 2 TMEM alloc, 4-11 row warps in two groups
+// of four (warps 4-7 and 8-11; each group has one thread per query row).  In
+// the S CTA the groups take alternate pages (one group's P transfer overlaps
+// the other's softmax); in the O CTA they take one half each of the 512
+// output columns.
+constexpr int kThreads = 384;
+constexpr int kRowThreads = 256;
+constexpr int kRowWarps = 8;  // row-warp barriers take one arrival per warp (lane 0, after __syncwarp)
 constexpr int kNS = 3;         // S accumulators in TMEM (S CTA)
 constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..287)
 constexpr int kCtrlBytes = 512;
+constexpr int kPrefetchAhead = 6;  // pages pulled into L2 ahead of the page the producer copies
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy output rescale: O is rescaled only when a row's running max grows by
@@ -72,6 +80,14 @@ struct Cfg {
   static constexpr int kSlotO = kNBoxLat * kBox;
   static constexpr int kNStS = kF8 ? 6 : 3;
   static constexpr int kNStO = kF8 ? 6 : 3;
+  // A ring slot may be filled by several copies ("parts", each with its own
+  // full/empty barrier) so that MMAs start before the whole page landed.
+  // Measured on GB300: three 24 KB copies per page instead of one 72 KB
+  // copy raise the copy latency about threefold, so a page is one copy.
+  static constexpr int kPartsS = 1;
+  static constexpr int kBoxesPartS = kF8 ? 4 : 9;   // boxes of the c_kv / whole-row map per copy
+  static constexpr int kPartsO = 1;
+  static constexpr int kBoxesPartO = kF8 ? 4 : 8;
   static constexpr int kPBytes = kRows * kPage * kEsz;  // one P tile
   static constexpr int kPRow = kPage * kEsz;            // bytes of one P row (128 or 64)
   static constexpr int kKStepsPe = kF8 ? 2 : 4;         // 32-byte K steps in the k_pe box
@@ -89,32 +105,60 @@ struct Cfg {
   static constexpr uint32_t kQLoCol = 144;              // TMEM column of the lo term
   static constexpr uint32_t kIdescQK = make_idesc(kF8, 128, 64, false, false);
   static constexpr uint32_t kIdescPV = make_idesc(kF8, 128, 256, false, true);
-  static constexpr int kMlOff = kNStS * kSlotS;         // S CTA: (m, l)[128]
-  static constexpr int kDataS = kMlOff + 2 * kRows * 4;
-  static constexpr int kPOff = kNStO * kSlotO;          // O CTA: P[2]
-  static constexpr int kAlphaOff = kPOff + 2 * kPBytes; // O CTA: alpha[2][128] f32 (sent with P)
-  static constexpr int kDataO = kAlphaOff + 2 * kRows * 4;
+  static constexpr int kMlOff = kNStS * kSlotS;          // S CTA: (m0, l0, m1, l1)[128], one pair per group
+  static constexpr int kMrefOff = kMlOff + 4 * kRows * 4;  // S CTA: running max after a page [2 parities][128]
+  static constexpr int kDataS = kMrefOff + 2 * kRows * 4;
+  // O CTA: P slots first (a slot's padding rows read on into what follows,
+  // which must be shared memory of this CTA), then the c_kv ring, then the
+  // alphas that come with each P
+  static constexpr int kPOff = 0;
+  static constexpr int kPRegion = kF8 ? 3 * 8192 : 4 * 8192;
+  static constexpr int kRingOffO = kPOff + kPRegion;
+  static constexpr int kAlphaOff = kRingOffO + kNStO * kSlotO;
+  static constexpr int kAlphaBytes = kF8 ? 3 * kRows * 4 : 2 * kRows * 4;
+  static constexpr int kDataO = kAlphaOff + kAlphaBytes;
   static constexpr int kData = kDataS > kDataO ? kDataS : kDataO;
   // dynamic smem = alignment slack + 1024-aligned data + control block
   static constexpr int kSmem = 1024 + kData + kCtrlBytes;
-  // bytes the S CTA sends per page: P tile + one alpha per row
-  static constexpr uint32_t kPTx = kPBytes + kRows * 4;
+  // bytes the S CTA sends per page and real query row: P row + its alpha
+  static constexpr uint32_t kPTxRow = kPRow + 4;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
+// P slots of a row block in the O CTA.  bf16: a P row is 128 bytes; with at
+// most 64 real rows a slot needs only 8 KB (the MMA's rows 64-127 read the
+// next 8 KB, whose results land in O rows that are never stored), so the
+// 32 KB region holds 4 slots, else 2 of 16 KB.  e4m3: 3 slots of 8 KB.
+struct PSlots {
+  int n;            // slots
+  uint32_t stride;  // bytes from one slot to the next
+  int arows;        // alpha entries per slot
+  __device__ PSlots(bool f8, int rows_real) {
+    if (f8) {
+      n = 3; stride = 8192; arows = kRows;
+    } else if (rows_real <= 64) {
+      n = 4; stride = 8192; arows = 64;
+    } else {
+      n = 2; stride = 16384; arows = kRows;
+    }
+  }
+};
+constexpr int kMaxPSlots = 4;
+
 struct __align__(8) Ctrl {
-  uint64_t kv_full[6];
-  uint64_t kv_empty[6];
+  uint64_t kv_full[9];   // one per ring part: slot * parts + part
+  uint64_t kv_empty[9];
   uint64_t s_full[kNS];
   uint64_t s_empty[kNS];
-  uint64_t q_full;
-  uint64_t p_full[2];
-  uint64_t p_empty[2];
+  uint64_t q_full[2];  // queries of the unit loaded, per QK issuer (even / odd pages)
+  uint64_t p_full[kMaxPSlots];
+  uint64_t p_empty[kMaxPSlots];
   uint64_t o_full;
   uint64_t o_empty;
-  uint64_t resc_done[2];
+  uint64_t resc_done[kMaxPSlots];
   uint64_t ml_full;
   uint64_t ml_empty;
+  uint64_t hb[2];  // S CTA: running max after page j published, per page parity (one group each)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -122,6 +166,7 @@ struct __align__(8) Ctrl {
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 struct Params {
+  const uint8_t* kv;       // cache pool (read only by the L2 prefetch; pages come by TMA)
   const uint8_t* q_nope;   // bf16
   const uint8_t* q_pe;     // bf16
   const int32_t* page_table;
@@ -255,12 +300,35 @@ struct UnitIter {
   }
 };
 
+// The slice's pages in processing order, one at a time.
+struct PageCursor {
+  UnitIter it;
+  Unit u;
+  int pg;
+  bool live;
+  __device__ void init(const Params& p, int c) {
+    it.init(p, c);
+    live = it.next(u);
+    pg = live ? u.p0 : 0;
+  }
+  __device__ bool next(int& b, int& page) {
+    while (live && pg >= u.p1) {
+      live = it.next(u);
+      if (live) pg = u.p0;
+    }
+    if (!live) return false;
+    b = u.b;
+    page = pg++;
+    return true;
+  }
+};
+
 // Which wait gave up, recorded (first one only) in status[1..3] of the
 // workspace: wait tag, page counter, (cluster << 16) | (rank << 8) | warp.
 enum WaitTag : int {
   kWaitProdEmptyS = 1, kWaitProdEmptyO, kWaitQFull, kWaitKvFullS, kWaitSEmpty, kWaitSFull, kWaitPEmptyS,
   kWaitMlEmpty, kWaitKvFullO, kWaitPFullO, kWaitOEmpty, kWaitRescDone, kWaitPFullCorr, kWaitPvPrev,
-  kWaitOFull, kWaitMlFull
+  kWaitOFull, kWaitMlFull, kWaitHandoff, kWaitSPrevUnit
 };
 
 __device__ __forceinline__ void raise_timeout(const Params& p, Ctrl* ctrl, uint32_t partner_rank, int tag,
@@ -283,56 +351,86 @@ __device__ __forceinline__ int32_t read_page_id(const Params& p, int b, int pg) 
   return pid;
 }
 
-// TMA producer shared by both roles: streams the slice's pages into a ring.
+// TMA producer shared by both roles: streams the slice's pages into a ring
+// of kNSt slots, each filled by kParts copies with their own barriers.
 template <bool kF8, bool kRoleS>
 __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const CUtensorMap* tm_kv,
-                             const CUtensorMap* tm_pe, int cid, uint32_t partner) {
+                             const CUtensorMap* tm_pe, int cid, uint32_t partner, bool prefetch) {
   using C = Cfg<kF8>;
   constexpr int kNSt = kRoleS ? C::kNStS : C::kNStO;
   constexpr int kSlot = kRoleS ? C::kSlotS : C::kSlotO;
+  constexpr int kParts = kRoleS ? C::kPartsS : C::kPartsO;
+  constexpr int kBoxes = kRoleS ? C::kBoxesPartS : C::kBoxesPartO;
+  constexpr uint32_t kPartBytes = static_cast<uint32_t>(kBoxes * C::kBox);
+  constexpr uint32_t kPageBytes = kPage * (kDL + kDR) * C::kEsz;
+  static_assert(kNSt * kParts <= 9, "ring parts");
   volatile int* abort = &ctrl->abort;
   UnitIter it;
   it.init(p, cid);
   Unit u;
   uint32_t j = 0;
   bool ok = true;
+  // copy i (page i / kParts, part i % kParts) uses ring part i % kNQ with
+  // phase (i / kNQ) & 1
+  constexpr uint32_t kNQ = kNSt * kParts;
+  uint32_t copies = 0;
+  // Pages kNSt .. are pulled into L2 kPrefetchAhead pages before their copy
+  // is issued, so that the copy (issued when a ring slot frees up) reads L2.
+  PageCursor ahead;
+  ahead.init(p, cid);
+  uint32_t pf = 0;
   while (ok && it.next(u)) {
-    for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+    for (int pg = u.p0; pg < u.p1 && ok; ++pg, ++j) {
+      if (prefetch) {
+        int pb, ppg;
+        while (pf < j + kPrefetchAhead && ahead.next(pb, ppg)) {
+          if (pf >= static_cast<uint32_t>(kNSt)) {
+            const int32_t pid = __ldg(p.page_table + static_cast<int64_t>(pb) * p.pt_stride + ppg);
+            if (pid >= 0 && pid < p.num_pages) prefetch_l2_bulk(p.kv + static_cast<int64_t>(pid) * kPageBytes, kPageBytes);
+          }
+          ++pf;
+        }
+      }
       const int st = j % kNSt;
       const uint32_t ph = (j / kNSt) & 1;
-      if (!mbar_wait(smem_u32(&ctrl->kv_empty[st]), ph ^ 1, abort, p.timeout_ns)) {
-        raise_timeout(p, ctrl, partner, kRoleS ? kWaitProdEmptyS : kWaitProdEmptyO, j);
-        ok = false;
-        break;
-      }
       const int32_t pid = read_page_id(p, u.b, pg);
-      const uint32_t bar = smem_u32(&ctrl->kv_full[st]);
-      uint8_t* slot = ring + st * kSlot;
-      mbar_expect_tx(bar, kSlot);
       const int y = pid * kPage;
-      // one 3-D box = the whole page (or its c_kv part) in box-major,
-      // 128-byte-swizzled order: per-copy overhead dominates small copies
-      tma_load_3d(smem_u32(slot), tm_kv, 0, y, 0, bar);
-      if constexpr (kRoleS && kF8) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_pe, kDL, y, bar);
+      uint8_t* slot = ring + st * kSlot;
+#pragma unroll
+      for (int part = 0; part < kParts; ++part) {
+        const int q = st * kParts + part;
+        if (!mbar_wait(smem_u32(&ctrl->kv_empty[q]), ph ^ 1, abort, p.timeout_ns)) {
+          raise_timeout(p, ctrl, partner, kRoleS ? kWaitProdEmptyS : kWaitProdEmptyO, j);
+          ok = false;
+          break;
+        }
+        const uint32_t bar = smem_u32(&ctrl->kv_full[q]);
+        const bool pe = kRoleS && kF8;  // e4m3 S CTA: the k_pe box comes by its own map
+        mbar_expect_tx(bar, kPartBytes + (pe ? static_cast<uint32_t>(C::kPeBytes) : 0u));
+        // 3-D boxes: kBoxes 128-byte columns x 64 token rows, box-major and
+        // 128-byte swizzled
+        tma_load_3d(smem_u32(slot + part * kPartBytes), tm_kv, 0, y, part * kBoxes, bar);
+        if (pe) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_pe, kDL, y, bar);
+        ++copies;
+      }
       MLA_TRACE_POINT(kRoleS ? 0 : 1, 0, j);
     }
   }
-  // Drain: every load issued into each stage must have landed before exit.
-  const uint32_t issued = j;
-  for (int st = 0; st < kNSt; ++st) {
-    if (static_cast<uint32_t>(st) >= issued) break;
-    const uint32_t last = issued - 1 - ((issued - 1 - st) % kNSt);  // last index with this stage
-    const uint32_t ph = (last / kNSt) & 1;
+  // Drain: every copy issued into each part must have landed before exit.
+  for (uint32_t q = 0; q < kNQ && q < copies; ++q) {
+    const uint32_t last = copies - 1 - ((copies - 1 - q) % kNQ);  // last copy into part q
+    const uint32_t ph = (last / kNQ) & 1;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(smem_u32(&ctrl->kv_full[st]), ph) && globaltimer_ns() - t0 < p.timeout_ns) {
+    while (!mbar_try_wait(smem_u32(&ctrl->kv_full[q]), ph) && globaltimer_ns() - t0 < p.timeout_ns) {
     }
   }
 }
 
 // Writes one row's final (unsplit) or partial (split) result.
+// Columns [256 * half, 256 * half + 256) of the row; half 0 also writes the lse.
 template <bool kF8>
-__device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g, int r, uint32_t taddr_row,
-                                          float m_log2, float l) {
+__device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g, int r, int half,
+                                          uint32_t taddr_row, float m_log2, float l) {
   const int rr = g * kRows + r;
   const bool real = rr < p.R;
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -346,7 +444,7 @@ __device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g,
     const int i = rr / p.H, h = rr % p.H;
     const int64_t orow = (static_cast<int64_t>(u.b) * p.Q + i) * p.H + h;
     uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDL * 2);
-    for (int c = 0; c < kDL; c += 16) {
+    for (int c = half * 256; c < half * 256 + 256; c += 16) {
       uint32_t v[16];
       tmem_ld16(taddr_row + c, v);
       tmem_wait_ld_tie(v);
@@ -362,11 +460,11 @@ __device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g,
         dst[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
     }
-    if (real) p.lse[orow] = lse_v;
+    if (real && half == 0) p.lse[orow] = lse_v;
   } else {
     const int64_t prow = (static_cast<int64_t>(u.slot) * p.G + g) * kRows + r;
     float4* dst = reinterpret_cast<float4*>(p.o_part + prow * kDL);
-    for (int c = 0; c < kDL; c += 16) {
+    for (int c = half * 256; c < half * 256 + 256; c += 16) {
       uint32_t v[16];
       tmem_ld16(taddr_row + c, v);
       tmem_wait_ld_tie(v);
@@ -377,7 +475,7 @@ __device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g,
                                        __uint_as_float(v[4 * k + 2]) * oscale, __uint_as_float(v[4 * k + 3]) * oscale);
       }
     }
-    if (real) p.lse_part[prow] = lse_v;
+    if (real && half == 0) p.lse_part[prow] = lse_v;
   }
 }
 
@@ -461,6 +559,28 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
   }
 }
 
+// e4m3 queries: the per-row scale load_q_row uses (amax / 448), computed by
+// the softmax group that does not load the queries itself.
+__device__ __forceinline__ float query_scale(const Params& p, int b, int g, int r) {
+  const int rr = g * kRows + r;
+  if (rr >= p.R) return 1.f;
+  const int i = rr / p.H, h = rr % p.H;
+  const int64_t row = (static_cast<int64_t>(b) * p.Q + i) * p.H + h;
+  const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
+  const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + row * kDR * 2);
+  float amax = 0.f;
+  for (int c = 0; c < 72; ++c) {
+    const uint4 v = c < 64 ? __ldg(qn + c) : __ldg(qp + (c - 64));
+    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  return amax > 0.f ? amax / 448.f : 1.f;
+}
+
 // ---------------------------------------------------------------- K1
 template <bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -479,25 +599,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 6; ++i) {
+    for (int i = 0; i < 9; ++i) {
       mbar_init(smem_u32(&ctrl->kv_full[i]), 1);
       mbar_init(smem_u32(&ctrl->kv_empty[i]), 1);
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(smem_u32(&ctrl->s_full[i]), 1);
-      mbar_init(smem_u32(&ctrl->s_empty[i]), 128);
+      mbar_init(smem_u32(&ctrl->s_empty[i]), kRowWarps / 2);  // the group that read the page
     }
-    mbar_init(smem_u32(&ctrl->q_full), 128);
-    for (int i = 0; i < 2; ++i) {
+    mbar_init(smem_u32(&ctrl->q_full[0]), kRowWarps / 2);  // half 0 loads the queries
+    mbar_init(smem_u32(&ctrl->q_full[1]), kRowWarps / 2);
+    for (int i = 0; i < kMaxPSlots; ++i) {
       mbar_init(smem_u32(&ctrl->p_full[i]), 1);  // one arm (expect_tx) by the O MMA warp + P bytes
       mbar_init(smem_u32(&ctrl->p_empty[i]), 1);
-      mbar_init(smem_u32(&ctrl->resc_done[i]), 128);
+      mbar_init(smem_u32(&ctrl->resc_done[i]), kRowWarps);
     }
     mbar_init(smem_u32(&ctrl->o_full), 1);
-    mbar_init(smem_u32(&ctrl->o_empty), 128);
-    mbar_init(smem_u32(&ctrl->ml_full), 128);
-    mbar_init(smem_u32(&ctrl->ml_empty), 128);
-    mbar_init(smem_u32(&ctrl->drain), 1);
+    mbar_init(smem_u32(&ctrl->o_empty), kRowWarps);
+    mbar_init(smem_u32(&ctrl->ml_full), kRowWarps);
+    mbar_init(smem_u32(&ctrl->ml_empty), kRowWarps);
+    mbar_init(smem_u32(&ctrl->hb[0]), kRowWarps / 2);
+    mbar_init(smem_u32(&ctrl->hb[1]), kRowWarps / 2);
+    mbar_init(smem_u32(&ctrl->drain), role_s ? 2 : 1);  // S CTA: one commit per QK issuer
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -519,60 +642,102 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (role_s) {
     // =========================== S CTA ===========================
     uint8_t* ring = data;
-    float* ml_buf = reinterpret_cast<float*>(data + C::kMlOff);
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, cid, partner);
-    } else if (warp == 1) {
+      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, cid, partner, rank == 0);
+    } else if (warp == 1 || warp == 3) {
+      // Two QK issuers, warp 1 for even pages and warp 3 for odd pages: one
+      // issuing thread sustains only about one N = 64 MMA per 55 cycles,
+      // two keep the tensor pipe full (32 cycles per MMA).
       if (lane == 0) {
+        const uint32_t mine = warp == 1 ? 0u : 1u;
         UnitIter it;
         it.init(p, cid);
         Unit u;
-        uint32_t j = 0, un = 0;
+        uint32_t j = 0, qn = 0;
         bool ok = true;
         int why = 0;
         while (ok && it.next(u)) {
-          if (!mbar_wait(smem_u32(&ctrl->q_full), un & 1, abort, p.timeout_ns)) { ok = false; why = kWaitQFull; break; }
+          // q_full[mine] completes once per unit holding a page of this
+          // issuer, and only those units are awaited: a unit without one is
+          // skipped (its queries are never read here)
+          const uint32_t npg = static_cast<uint32_t>(u.p1 - u.p0);
+          if (npg < 2 && (j & 1u) != mine) {
+            j += npg;
+            continue;
+          }
+          if (!mbar_wait(smem_u32(&ctrl->q_full[mine]), qn & 1, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitQFull;
+            break;
+          }
+          ++qn;
           for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+            if ((j & 1u) != mine) continue;
             const int st = j % C::kNStS;
             const int sb = j % kNS;
-            if (!mbar_wait(smem_u32(&ctrl->kv_full[st]), (j / C::kNStS) & 1, abort, p.timeout_ns)) {
-              ok = false;
-              why = kWaitKvFullS;
-              break;
-            }
+            const uint32_t kph = (j / C::kNStS) & 1;
             if (!mbar_wait(smem_u32(&ctrl->s_empty[sb]), ((j / kNS) & 1) ^ 1, abort, p.timeout_ns)) {
               ok = false;
               why = kWaitSEmpty;
               break;
             }
-            MLA_TRACE_POINT(0, 1, j);
-            tc_fence_after();
             // descriptors of box 0 / the k_pe box at K step 0; a K step adds
             // 32 bytes (2 in the >>4 address field), a box adds 8 KB (512)
             const uint32_t slot_addr = smem_u32(ring + st * C::kSlotS);
             const uint64_t dlat = smem_desc(slot_addr, 16, 1024, kSwizzle128B);
-            const uint64_t dpe = smem_desc(slot_addr + C::kNBoxLat * C::kBox, 16, C::kPeSbo, C::kPeSwz);
             const uint32_t dcol = tmem + kSCol0 + sb * 64;
+            if constexpr (!kF8) {
+              // 9 boxes (8 of c_kv, 1 of k_pe) x 4 K steps, part by part
 #pragma unroll
-            for (int term = 0; term < C::kQSplit; ++term) {
-              const uint32_t qcol = tmem + (term ? C::kQLoCol : 0u);
+              for (int part = 0; part < C::kPartsS; ++part) {
+                const int q = st * C::kPartsS + part;
+                if (!mbar_wait(smem_u32(&ctrl->kv_full[q]), kph, abort, p.timeout_ns)) {
+                  ok = false;
+                  why = kWaitKvFullS;
+                  break;
+                }
+                if (part == 0) MLA_TRACE_POINT(0, 1, j);
+                tc_fence_after();
 #pragma unroll
-              for (int d = 0; d < C::kNBoxLat; ++d) {
+                for (int dd = 0; dd < C::kBoxesPartS; ++dd) {
+                  const int d = part * C::kBoxesPartS + dd;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  mma_ts<kF8>(dcol, qcol + d * 32 + k * 8, dlat + static_cast<uint64_t>(d * 512 + k * 2),
-                              C::kIdescQK, (term | d | k) ? 1u : 0u);
+                  for (int k = 0; k < 4; ++k)
+                    mma_ts<false>(dcol, tmem + d * 32 + k * 8, dlat + static_cast<uint64_t>(d * 512 + k * 2),
+                                  C::kIdescQK, (d | k) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&ctrl->kv_empty[q]));
               }
+              if (!ok) break;
+            } else {
+              if (!mbar_wait(smem_u32(&ctrl->kv_full[st]), kph, abort, p.timeout_ns)) {
+                ok = false;
+                why = kWaitKvFullS;
+                break;
+              }
+              MLA_TRACE_POINT(0, 1, j);
+              tc_fence_after();
+              const uint64_t dpe = smem_desc(slot_addr + C::kNBoxLat * C::kBox, 16, C::kPeSbo, C::kPeSwz);
 #pragma unroll
-              for (int k = 0; k < C::kKStepsPe; ++k)
-                mma_ts<kF8>(dcol, qcol + C::kNBoxLat * 32 + k * 8, dpe + static_cast<uint64_t>(k * 2), C::kIdescQK,
-                            1u);
+              for (int term = 0; term < C::kQSplit; ++term) {
+                const uint32_t qcol = tmem + (term ? C::kQLoCol : 0u);
+#pragma unroll
+                for (int d = 0; d < C::kNBoxLat; ++d) {
+#pragma unroll
+                  for (int k = 0; k < 4; ++k)
+                    mma_ts<true>(dcol, qcol + d * 32 + k * 8, dlat + static_cast<uint64_t>(d * 512 + k * 2),
+                                 C::kIdescQK, (term | d | k) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < C::kKStepsPe; ++k)
+                  mma_ts<true>(dcol, qcol + C::kNBoxLat * 32 + k * 8, dpe + static_cast<uint64_t>(k * 2),
+                               C::kIdescQK, 1u);
+              }
+              mma_commit(smem_u32(&ctrl->kv_empty[st]));
             }
-            mma_commit(smem_u32(&ctrl->kv_empty[st]));
             mma_commit(smem_u32(&ctrl->s_full[sb]));
             MLA_TRACE_POINT(0, 2, j);
           }
-          ++un;
         }
         if (!ok) raise_timeout(p, ctrl, partner, why, j);
         mma_commit(smem_u32(&ctrl->drain));
@@ -581,16 +746,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp >= 4) {
-      // ---- softmax: thread r owns query row r of the block
-      const int r = threadIdx.x - 128;
+      // ---- softmax: group gg (warps 4-7: 0, warps 8-11: 1) takes the pages
+      // j with j % 2 == gg; its thread r owns query row r.  The running max
+      // (the reference of P and of O) is handed from page j to page j + 1
+      // through mref_buf and hb; each group keeps its own partial sum, in
+      // the frame of the running max after its latest page.
+      const int r = (warp & 3) * 32 + lane;
+      const int gg = (warp - 4) >> 2;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t p_remote = mapa(smem_u32(data + C::kPOff), partner);
       const uint32_t alpha_remote = mapa(smem_u32(data + C::kAlphaOff), partner);
-      const uint32_t pfull_remote0 = mapa(smem_u32(&ctrl->p_full[0]), partner);
-      const uint32_t pfull_remote1 = mapa(smem_u32(&ctrl->p_full[1]), partner);
       const uint32_t mlfull_remote = mapa(smem_u32(&ctrl->ml_full), partner);
+      float* mref_buf = reinterpret_cast<float*>(data + C::kMrefOff);
       const int rr = g * kRows + r;
-      const int qi = rr < p.R ? rr / p.H : p.Q - 1;
+      const bool real = rr < p.R;  // rows past H * q_len are padding: nothing of theirs is sent
+      const PSlots ps(kF8, p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
+      const int qi = real ? rr / p.H : p.Q - 1;
       UnitIter it;
       it.init(p, cid);
       Unit u;
@@ -598,13 +769,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int why = 0;
       while (ok && it.next(u)) {
-        const float qs = load_q_row<kF8>(p, u.b, g, r, tmem + lane_base);
-        tc_fence_before();
-        mbar_arrive(smem_u32(&ctrl->q_full));
-        const float c2 = p.scale * kLog2e * (kF8 ? qs * p.kv_scale : 1.f);
+        const int npg = u.p1 - u.p0;
+        float qs = 1.f;
+        if (gg == 0) {
+          // the queries of this unit replace the previous unit's in TMEM once
+          // every QK of that unit is done: the S of its last two pages (one
+          // per issuer) has landed
+          for (uint32_t back = 1; back <= 2 && ok; ++back) {
+            if (j < back) break;
+            const uint32_t jb = j - back;
+            if (!mbar_wait_warp(smem_u32(&ctrl->s_full[jb % kNS]), (jb / kNS) & 1, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitSPrevUnit;
+            }
+          }
+          if (!ok) break;
+          qs = load_q_row<kF8>(p, u.b, g, r, tmem + lane_base);
+          tc_fence_before();
+          __syncwarp();
+          // release the queries to the QK issuer(s) of this unit's pages
+          if (lane == 0 && (npg >= 2 || (j & 1u) == 0)) mbar_arrive(smem_u32(&ctrl->q_full[0]));
+          if (lane == 0 && (npg >= 2 || (j & 1u) == 1)) mbar_arrive(smem_u32(&ctrl->q_full[1]));
+        } else if constexpr (kF8) {
+          qs = query_scale(p, u.b, g, r);
+        }
+        const float c2 = p.scale * kLog2e * (kF8 ? qs * p.kv_scale : 1.f);  // log2-domain score scale
         const int nvis = u.L - p.Q + qi + 1;
-        float m_ref = kMinusBig, l = 0.f;
+        float m_run = kMinusBig, l = 0.f;  // this group's frame and partial sum
         for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+          if ((j & 1u) != static_cast<uint32_t>(gg)) continue;
           const int sb = j % kNS;
           if (!mbar_wait_warp(smem_u32(&ctrl->s_full[sb]), (j / kNS) & 1, abort, p.timeout_ns)) {
             ok = false;
@@ -619,106 +812,133 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld_tie(v[q4]);
           tc_fence_before();
-          mbar_arrive(smem_u32(&ctrl->s_empty[sb]));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->s_empty[sb]));
+          if (r == 0) MLA_TRACE_POINT(0, 7, j);
           const int t0 = pg * kPage;
-          // every key of the page visible to this row: no per-key masking
+          // every key of the page visible to the row: no per-key masking
           const bool full = t0 + kPage <= nvis;
 #define MLA_S(t) __uint_as_float(v[(t) >> 4][(t) & 15])
-          float mxr = -INFINITY;  // max of the raw scores (c2 > 0, so scaling commutes with max)
+          // max of the raw scores (c2 > 0, so scaling commutes with max);
+          // unused slots (even NaN) never pass the mask
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
           if (full) {
 #pragma unroll
-            for (int t = 0; t < 64; ++t) mxr = fmaxf(mxr, MLA_S(t));
+            for (int t = 0; t < 64; ++t) m4[t & 3] = fmaxf(m4[t & 3], MLA_S(t));
           } else {
 #pragma unroll
             for (int t = 0; t < 64; ++t)
-              if (t0 + t < nvis) mxr = fmaxf(mxr, MLA_S(t));  // unused slots (even NaN) never pass
+              if (t0 + t < nvis) m4[t & 3] = fmaxf(m4[t & 3], MLA_S(t));
           }
-          const float mx = mxr * c2;
+          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;
+          // running max after page j - 1 (a unit starts from scratch); the
+          // wait is made on every page so the chain of hand-offs stays strict
+          float m_prev = kMinusBig;
+          if (j > 0) {
+            const uint32_t jp = j - 1;
+            if (!mbar_wait_warp(smem_u32(&ctrl->hb[jp & 1]), (jp >> 1) & 1, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitHandoff;
+              break;
+            }
+            if (pg != u.p0) m_prev = mref_buf[(jp & 1) * kRows + r];
+          }
           const bool first = pg == u.p0;  // O is overwritten on a unit's first page
-          float alpha = 1.f;
-          if (mx > m_ref + SoftmaxCfg<kF8>::kThreshold) {
-            alpha = first ? 0.f : ex2_approx(m_ref - mx);
+          float m_ref = m_prev, alpha = 1.f;
+          if (mx > m_prev + SoftmaxCfg<kF8>::kThreshold) {
+            alpha = first ? 0.f : ex2_approx(m_prev - mx);
             m_ref = mx;
           }
-          const int pb = j & 1;
-          const float nm = SoftmaxCfg<kF8>::kShift - m_ref;  // P = 2^(s * c2 - m_ref + shift)
-          float sum = 0.f;
-          uint32_t pw[kF8 ? 16 : 32];
-          auto prob = [&](int t) {
-            const float e = ex2_approx(fmaf(MLA_S(t), c2, nm));
-            return (full || t0 + t < nvis) ? e : 0.f;
-          };
-          if constexpr (!kF8) {
-#pragma unroll
-            for (int t = 0; t < 64; t += 2) {
-              const float a = prob(t), b = prob(t + 1);
-              sum += a + b;  // bf16 rounding of P changes l by < 2^-9 relative
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
-              pw[t / 2] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-          } else {
-#pragma unroll
-            for (int t = 0; t < 64; t += 4) {
-              const __nv_fp8x2_storage_t lo =
-                  __nv_cvt_float2_to_fp8x2(make_float2(prob(t), prob(t + 1)), __NV_SATFINITE, __NV_E4M3);
-              const __nv_fp8x2_storage_t hi =
-                  __nv_cvt_float2_to_fp8x2(make_float2(prob(t + 2), prob(t + 3)), __NV_SATFINITE, __NV_E4M3);
-              // l sums the e4m3-rounded P actually multiplied into O
-              const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
-              const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
-              const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&hl));
-              const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hh));
-              sum += (fl.x + fl.y) + (fh.x + fh.y);
-              pw[t / 4] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-            }
-          }
-#undef MLA_S
-          l = l * alpha + sum;
-          // P slot pb is free once the O CTA finished PV of page j-2
-          if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[pb]), ((j >> 1) & 1) ^ 1, abort, p.timeout_ns)) {
+          mref_buf[(j & 1) * kRows + r] = m_ref;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->hb[j & 1]));
+          if (r == 0) MLA_TRACE_POINT(0, 8, j);
+          l *= ex2_approx(m_run - m_ref);  // m_run <= m_ref: the partial sum moves to the new frame
+          m_run = m_ref;
+          // P slot ps_slot is free once the O CTA finished PV of page j - ps.n
+          const int ps_slot = static_cast<int>(j % static_cast<uint32_t>(ps.n));
+          const uint32_t ps_phase = (j / static_cast<uint32_t>(ps.n)) & 1;
+          if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[ps_slot]), ps_phase ^ 1, abort, p.timeout_ns)) {
             ok = false;
             why = kWaitPEmptyS;
             break;
           }
           if (r == 0) MLA_TRACE_POINT(0, 4, j);
-          // P row (swizzled for the MMA) and alpha go straight into the O
-          // CTA's shared memory; the bytes complete on its p_full barrier
-          const uint32_t bar = pb ? pfull_remote1 : pfull_remote0;
-          const uint32_t prow = p_remote + pb * C::kPBytes + r * C::kPRow;
+          // P (swizzled for the MMA) is computed 16 bytes at a time and each
+          // chunk goes straight into the O CTA's shared memory, completing
+          // bytes on its p_full barrier; then the row's alpha
+          const float nm = SoftmaxCfg<kF8>::kShift - m_ref;  // P = 2^(s * c2 - m_ref + shift)
+          const uint32_t bar = mapa(smem_u32(&ctrl->p_full[ps_slot]), partner);
+          const uint32_t prow = p_remote + ps_slot * ps.stride + r * C::kPRow;
+          auto prob = [&](int t) {
+            const float e = ex2_approx(fmaf(MLA_S(t), c2, nm));
+            return (full || t0 + t < nvis) ? e : 0.f;
+          };
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
           if constexpr (!kF8) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              st_async_v4(prow + ((c ^ (r & 7)) << 4),
-                          make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]), bar);
+            for (int c = 0; c < 8; ++c) {  // keys 8c .. 8c + 7
+              uint32_t w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float a = prob(8 * c + 2 * k), b = prob(8 * c + 2 * k + 1);
+                s4[k] += a + b;  // bf16 rounding of P changes l by < 2^-9 relative
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
+                w[k] = *reinterpret_cast<uint32_t*>(&b2);
+              }
+              if (real) st_async_v4(prow + ((c ^ (r & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]), bar);
+            }
           } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              st_async_v4(prow + ((c ^ ((r >> 1) & 3)) << 4),
-                          make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]), bar);
+            for (int c = 0; c < 4; ++c) {  // keys 16c .. 16c + 15
+              uint32_t w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int t = 16 * c + 4 * k;
+                const __nv_fp8x2_storage_t lo =
+                    __nv_cvt_float2_to_fp8x2(make_float2(prob(t), prob(t + 1)), __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t hi =
+                    __nv_cvt_float2_to_fp8x2(make_float2(prob(t + 2), prob(t + 3)), __NV_SATFINITE, __NV_E4M3);
+                // l sums the e4m3-rounded P actually multiplied into O
+                const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
+                const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+                const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&hl));
+                const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hh));
+                s4[k] += (fl.x + fl.y) + (fh.x + fh.y);
+                w[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+              }
+              if (real) st_async_v4(prow + ((c ^ ((r >> 1) & 3)) << 4), make_uint4(w[0], w[1], w[2], w[3]), bar);
+            }
           }
-          st_async_b32(alpha_remote + (pb * kRows + r) * 4, __float_as_uint(alpha), bar);
+#undef MLA_S
+          if (real) st_async_b32(alpha_remote + (ps_slot * ps.arows + r) * 4, __float_as_uint(alpha), bar);
+          l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
           if (r == 0) MLA_TRACE_POINT(0, 5, j);
         }
         if (!ok) break;
-        // hand the row's (running max, sum) to the O CTA for the epilogue
+        // hand this group's (frame, partial sum) of the row to the O CTA
         if (!mbar_wait_warp(smem_u32(&ctrl->ml_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
           ok = false;
           why = kWaitMlEmpty;
           break;
         }
-        ml_buf[2 * r] = m_ref;
-        ml_buf[2 * r + 1] = l;
-        mbar_arrive_cluster(mlfull_remote);
+        float* ml_buf = reinterpret_cast<float*>(data + C::kMlOff);
+        ml_buf[4 * r + 2 * gg] = m_run;
+        ml_buf[4 * r + 2 * gg + 1] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mlfull_remote);
         ++un;
       }
       if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
     }
   } else {
     // =========================== O CTA ===========================
-    uint8_t* ring = data;
+    uint8_t* ring = data + C::kRingOffO;
     uint8_t* pbuf = data + C::kPOff;
+    const int rows_real = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
+    const PSlots ps(kF8, rows_real);
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, cid, partner);
+      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, cid, partner, false);
     } else if (warp == 1) {
       UnitIter it;
       it.init(p, cid);
@@ -727,44 +947,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int why = 0;
       const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << partner));
-      if (lane == 0) {  // arm the P barriers for pages 0 and 1 (bytes may land before or after)
-        mbar_expect_tx(smem_u32(&ctrl->p_full[0]), C::kPTx);
-        mbar_expect_tx(smem_u32(&ctrl->p_full[1]), C::kPTx);
+      // the S CTA sends the P rows (and alphas) of real query rows only
+      const uint32_t ptx = static_cast<uint32_t>(rows_real) * C::kPTxRow;
+      if (lane == 0) {  // arm the P barriers of the first pages (bytes may land before or after)
+        for (int i = 0; i < ps.n; ++i) mbar_expect_tx(smem_u32(&ctrl->p_full[i]), ptx);
       }
       while (ok && it.next(u)) {
         for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
           const int st = j % C::kNStO;
-          const int pb = j & 1;
+          const uint32_t kph = (j / C::kNStO) & 1;
+          const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
+          const uint32_t pph = (j / static_cast<uint32_t>(ps.n)) & 1;
           uint8_t* slot = ring + st * C::kSlotO;
-          if (!mbar_wait_warp(smem_u32(&ctrl->kv_full[st]), (j / C::kNStO) & 1, abort, p.timeout_ns)) {
+          const int valid = u.L - pg * kPage;
+          // waits for ring part `part` of this page; token rows past the
+          // sequence end may hold anything (even NaN): they are zeroed so
+          // that P = 0 there cannot turn into 0 * NaN
+          auto part_ready = [&](int part) -> bool {
+            if (!mbar_wait_warp(smem_u32(&ctrl->kv_full[st * C::kPartsO + part]), kph, abort, p.timeout_ns))
+              return false;
+            if (valid < kPage) {
+              const int v0 = valid > 0 ? valid : 0;
+              const int nrows = kPage - v0;
+              for (int idx = lane; idx < C::kBoxesPartO * nrows * 8; idx += 32) {
+                const int chunk = idx & 7;
+                const int rowi = (idx >> 3) % nrows + v0;
+                const int box = part * C::kBoxesPartO + (idx >> 3) / nrows;
+                *reinterpret_cast<uint4*>(slot + box * C::kBox + rowi * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_cta();
+              __syncwarp();
+            }
+            return true;
+          };
+          if (!part_ready(0)) {
             ok = false;
             why = kWaitKvFullO;
             break;
           }
           if (lane == 0) MLA_TRACE_POINT(1, 1, j);
-          const int valid = u.L - pg * kPage;
-          if (valid < kPage) {
-            // slots past the sequence end may hold anything (even NaN): zero
-            // them so that P = 0 there cannot turn into 0 * NaN
-            const int v0 = valid > 0 ? valid : 0;
-            const int nrows = kPage - v0;
-            for (int idx = lane; idx < C::kNBoxLat * nrows * 8; idx += 32) {
-              const int chunk = idx & 7;
-              const int rowi = (idx >> 3) % nrows + v0;
-              const int box = (idx >> 3) / nrows;
-              *reinterpret_cast<uint4*>(slot + box * C::kBox + rowi * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_cta();
-            __syncwarp();
-          }
-          if (!mbar_wait_warp(smem_u32(&ctrl->p_full[pb]), (j >> 1) & 1, abort, p.timeout_ns)) {
+          if (!mbar_wait_warp(smem_u32(&ctrl->p_full[pb]), pph, abort, p.timeout_ns)) {
             ok = false;
             why = kWaitPFullO;
             break;
           }
-          // phase for page j done: arm this P slot for page j + 2.  Its bytes
-          // cannot come earlier: the S CTA sends them only after PV(j) ended.
-          if (lane == 0) mbar_expect_tx(smem_u32(&ctrl->p_full[pb]), C::kPTx);
+          // phase for page j done: arm this P slot for page j + ps.n.  Its
+          // bytes cannot come earlier: the S CTA sends them only after PV(j)
+          // ended.
+          if (lane == 0) mbar_expect_tx(smem_u32(&ctrl->p_full[pb]), ptx);
           if (lane == 0) MLA_TRACE_POINT(1, 2, j);
           const bool first = pg == u.p0;
           if (first && !mbar_wait_warp(smem_u32(&ctrl->o_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
@@ -772,26 +1002,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             why = kWaitOEmpty;
             break;
           }
-          if (!mbar_wait_warp(smem_u32(&ctrl->resc_done[pb]), (j >> 1) & 1, abort, p.timeout_ns)) {
+          if (!mbar_wait_warp(smem_u32(&ctrl->resc_done[pb]), pph, abort, p.timeout_ns)) {
             ok = false;
             why = kWaitRescDone;
             break;
           }
           fence_proxy_async_cta();
           tc_fence_after();
-          if (lane == 0) {
-            const uint64_t dp = smem_desc(smem_u32(pbuf + pb * C::kPBytes), 16, C::kPSbo, C::kPSwz);
-            const uint64_t dv = smem_desc(smem_u32(slot), C::kBox, 1024, kSwizzle128B);
+          const uint64_t dp = smem_desc(smem_u32(pbuf + pb * ps.stride), 16, C::kPSbo, C::kPSwz);
+          const uint64_t dv = smem_desc(smem_u32(slot), C::kBox, 1024, kSwizzle128B);
+          // O[:, 256h .. 256h + 255] += P V[:, 256h ..]: one N half after the other,
+          // so the first c_kv part is consumed (and released) first
 #pragma unroll
-            for (int k = 0; k < C::kPvKSteps; ++k) {
-              const uint32_t acc = (first && k == 0) ? 0u : 1u;
+          for (int h = 0; h < 2; ++h) {
+            if (h > 0 && C::kPartsO > 1) {
+              if (!part_ready(1)) {
+                ok = false;
+                why = kWaitKvFullO;
+                break;
+              }
+              tc_fence_after();
+            }
+            if (lane == 0) {
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
+              for (int k = 0; k < C::kPvKSteps; ++k)
                 mma_ss<kF8>(tmem + h * 256, dp + static_cast<uint64_t>(k * 2),
                             dv + static_cast<uint64_t>((h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes) >> 4),
-                            C::kIdescPV, acc);
+                            C::kIdescPV, (first && k == 0) ? 0u : 1u);
+              if (C::kPartsO > 1) mma_commit(smem_u32(&ctrl->kv_empty[st * C::kPartsO + h]));
             }
-            mma_commit(smem_u32(&ctrl->kv_empty[st]));
+            __syncwarp();
+          }
+          if (!ok) break;
+          if (lane == 0) {
+            if (C::kPartsO == 1) mma_commit(smem_u32(&ctrl->kv_empty[st]));
             mma_commit_multicast(smem_u32(&ctrl->p_empty[pb]), mask);
             if (pg == u.p1 - 1) mma_commit(smem_u32(&ctrl->o_full));
             MLA_TRACE_POINT(1, 3, j);
@@ -809,9 +1053,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp >= 4) {
-      // ---- correction (lazy O rescale) + epilogue: thread r owns row r
-      const int r = threadIdx.x - 128;
+      // ---- correction (lazy O rescale) + epilogue: threads (half h, r) own
+      // output columns [256h, 256h + 256) of row r
+      const int r = (warp & 3) * 32 + lane;
+      const int half = (warp - 4) >> 2;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t tcols = tmem + lane_base + half * 256;
+      const bool real = g * kRows + r < p.R;
       const float* alpha_buf = reinterpret_cast<const float*>(data + C::kAlphaOff);
       const uint32_t ml_remote = mapa(smem_u32(data + C::kMlOff), partner);
       const uint32_t mlempty_remote = mapa(smem_u32(&ctrl->ml_empty), partner);
@@ -823,39 +1071,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       int why = 0;
       while (ok && it.next(u)) {
         for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
-          const int pb = j & 1;
-          if (!mbar_wait_warp(smem_u32(&ctrl->p_full[pb]), (j >> 1) & 1, abort, p.timeout_ns)) {
+          const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
+          if (!mbar_wait_warp(smem_u32(&ctrl->p_full[pb]), (j / static_cast<uint32_t>(ps.n)) & 1, abort,
+                              p.timeout_ns)) {
             ok = false;
             why = kWaitPFullCorr;
             break;
           }
-          if (r == 0) MLA_TRACE_POINT(1, 4, j);
-          const float a = alpha_buf[pb * kRows + r];
+          if (r == 0 && half == 0) MLA_TRACE_POINT(1, 4, j);
+          // padding rows receive no alpha (their O rows are never stored)
+          const float a = real ? alpha_buf[pb * ps.arows + r] : 1.f;
           if (pg != u.p0 && __any_sync(0xffffffffu, a != 1.f)) {
             // wait until PV of the previous page has landed in O, then rescale
             const uint32_t jp = j - 1;
-            if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[jp & 1]), (jp >> 1) & 1, abort, p.timeout_ns)) {
+            const uint32_t np = static_cast<uint32_t>(ps.n);
+            if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[jp % np]), (jp / np) & 1, abort, p.timeout_ns)) {
               ok = false;
               why = kWaitPvPrev;
               break;
             }
             tc_fence_after();
-            {
-              for (int c = 0; c < kDL; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tmem + lane_base + c, v);
-                tmem_wait_ld_tie(v);
+            for (int c = 0; c < 256; c += 16) {
+              uint32_t v[16];
+              tmem_ld16(tcols + c, v);
+              tmem_wait_ld_tie(v);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * a);
-                tmem_st16(tmem + lane_base + c, v);
-              }
-              tmem_wait_st();
+              for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * a);
+              tmem_st16(tcols + c, v);
             }
+            tmem_wait_st();
           }
           // acknowledge page j (rescaled or not); PV of page j waits for this
           tc_fence_before();
-          mbar_arrive(smem_u32(&ctrl->resc_done[pb]));
-          if (r == 0) MLA_TRACE_POINT(1, 5, j);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->resc_done[pb]));
+          if (r == 0 && half == 0) MLA_TRACE_POINT(1, 5, j);
         }
         if (!ok) break;
         // epilogue for this unit
@@ -870,14 +1120,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const float m_log2 = __uint_as_float(ld_cluster_u32(ml_remote + 8 * r));
-        const float l = __uint_as_float(ld_cluster_u32(ml_remote + 8 * r + 4));
-        mbar_arrive_cluster(mlempty_remote);
-        if (r == 0) MLA_TRACE_POINT(1, 6, un);
-        store_row<kF8>(p, u, g, r, tmem + lane_base, m_log2, l);
-        if (r == 0) MLA_TRACE_POINT(1, 7, un);
+        // the two softmax groups' (frame, partial sum); O is in the frame of
+        // the later one, which is the larger (the running max never drops)
+        const float m0 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r));
+        const float l0 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 4));
+        const float m1 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 8));
+        const float l1 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 12));
+        const float m_log2 = fmaxf(m0, m1);
+        const float l = l0 * ex2_approx(m0 - m_log2) + l1 * ex2_approx(m1 - m_log2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mlempty_remote);
+        if (r == 0 && half == 0) MLA_TRACE_POINT(1, 6, un);
+        store_row<kF8>(p, u, g, r, half, tmem + lane_base, m_log2, l);
+        if (r == 0 && half == 0) MLA_TRACE_POINT(1, 7, un);
         tc_fence_before();
-        mbar_arrive(smem_u32(&ctrl->o_empty));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl->o_empty));
         ++un;
       }
       if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
@@ -991,7 +1249,9 @@ __global__ void __launch_bounds__(128) mla_gather_kernel(const __grid_constant__
   if (threadIdx.x == 0) {
     // exactly the loads of the decode kernel's S CTA
     mbar_expect_tx(smem_u32(bar), C::kSlotS);
-    tma_load_3d(smem_u32(page), &tm_s, 0, pid * kPage, 0, smem_u32(bar));
+    for (int part = 0; part < C::kPartsS; ++part)
+      tma_load_3d(smem_u32(page + part * C::kBoxesPartS * C::kBox), &tm_s, 0, pid * kPage, part * C::kBoxesPartS,
+                  smem_u32(bar));
     if constexpr (kF8) tma_load_2d(smem_u32(page + C::kNBoxLat * C::kBox), &tm_pe, kDL, pid * kPage, smem_u32(bar));
   }
   if (!mbar_wait(smem_u32(bar), 0, abort_flag, gp.timeout_ns)) {

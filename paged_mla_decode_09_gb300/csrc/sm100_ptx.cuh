@@ -153,6 +153,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
 
 // 2-D tiled TMA load into this CTA's shared memory, completion counted in
 // bytes on `bar`.  x is the innermost coordinate (elements).
+// Pulls `bytes` (a multiple of 16) of global memory at `gaddr` (16-byte
+// aligned) into L2 without a destination in shared memory.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gaddr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gaddr)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
