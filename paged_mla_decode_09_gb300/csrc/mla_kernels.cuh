@@ -93,8 +93,16 @@ struct Cfg {
   static constexpr int kKStepsPe = kF8 ? 2 : 4;         // 32-byte K steps in the k_pe box
   static constexpr uint32_t kPeSwz = kF8 ? kSwizzle64B : kSwizzle128B;
   static constexpr uint32_t kPeSbo = kF8 ? 512 : 1024;
-  static constexpr uint32_t kPSwz = kF8 ? kSwizzle64B : kSwizzle128B;
-  static constexpr uint32_t kPSbo = kF8 ? 512 : 1024;
+  // P tile: K-major without swizzle.  Core matrices of 8 rows x 16 bytes
+  // (8 keys bf16, 16 keys e4m3); the 16-byte chunk c of row r sits at
+  // (r / 8) * kPSbo + c * kPLbo + (r % 8) * 16, so chunk c of 8 consecutive
+  // rows is 128 contiguous bytes and a warp storing chunk c of its 32 rows
+  // into the O CTA writes four whole 128-byte lines (one row per thread and
+  // a swizzled tile would touch 32 lines with 16 bytes each).
+  static constexpr uint32_t kPSwz = kSwizzleNone;
+  static constexpr uint32_t kPLbo = 128;                // next core matrix along K
+  static constexpr uint32_t kPSbo = kF8 ? 512 : 1024;   // next 8-row group
+  static constexpr int kPChunks = kF8 ? 4 : 8;          // 16-byte chunks per P row
   static constexpr int kPvKSteps = kF8 ? 2 : 4;         // K = 64 tokens in steps of 32 (e4m3) / 16 (bf16)
   static constexpr int kVKStepBytes = kF8 ? 4096 : 2048;
   static constexpr int kVBoxesHalf = kF8 ? 2 : 4;       // boxes covering 256 output columns
@@ -150,7 +158,7 @@ struct __align__(8) Ctrl {
   uint64_t kv_empty[9];
   uint64_t s_full[kNS];
   uint64_t s_empty[kNS];
-  uint64_t q_full[2];  // queries of the unit loaded, per QK issuer (even / odd pages)
+  uint64_t q_full[kNS];  // queries of the unit loaded, per QK issuer (page j: issuer j % kNS)
   uint64_t p_full[kMaxPSlots];
   uint64_t p_empty[kMaxPSlots];
   uint64_t o_full;
@@ -159,6 +167,8 @@ struct __align__(8) Ctrl {
   uint64_t ml_full;
   uint64_t ml_empty;
   uint64_t hb[2];  // S CTA: running max after page j published, per page parity (one group each)
+  uint64_t pv_ready;  // O CTA: page j is ready for PV (waiter warp -> MMA warp)
+  uint64_t pv_taken;  // O CTA: the MMA warp took page j (keeps the waiter one page ahead at most)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -328,7 +338,7 @@ struct PageCursor {
 enum WaitTag : int {
   kWaitProdEmptyS = 1, kWaitProdEmptyO, kWaitQFull, kWaitKvFullS, kWaitSEmpty, kWaitSFull, kWaitPEmptyS,
   kWaitMlEmpty, kWaitKvFullO, kWaitPFullO, kWaitOEmpty, kWaitRescDone, kWaitPFullCorr, kWaitPvPrev,
-  kWaitOFull, kWaitMlFull, kWaitHandoff, kWaitSPrevUnit
+  kWaitOFull, kWaitMlFull, kWaitHandoff, kWaitSPrevUnit, kWaitPvReady, kWaitPvTaken
 };
 
 __device__ __forceinline__ void raise_timeout(const Params& p, Ctrl* ctrl, uint32_t partner_rank, int tag,
@@ -607,8 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->s_full[i]), 1);
       mbar_init(smem_u32(&ctrl->s_empty[i]), kRowWarps / 2);  // the group that read the page
     }
-    mbar_init(smem_u32(&ctrl->q_full[0]), kRowWarps / 2);  // half 0 loads the queries
-    mbar_init(smem_u32(&ctrl->q_full[1]), kRowWarps / 2);
+    for (int i = 0; i < kNS; ++i) mbar_init(smem_u32(&ctrl->q_full[i]), kRowWarps / 2);  // group 0 loads queries
     for (int i = 0; i < kMaxPSlots; ++i) {
       mbar_init(smem_u32(&ctrl->p_full[i]), 1);  // one arm (expect_tx) by the O MMA warp + P bytes
       mbar_init(smem_u32(&ctrl->p_empty[i]), 1);
@@ -618,9 +627,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&ctrl->o_empty), kRowWarps);
     mbar_init(smem_u32(&ctrl->ml_full), kRowWarps);
     mbar_init(smem_u32(&ctrl->ml_empty), kRowWarps);
+    mbar_init(smem_u32(&ctrl->pv_ready), 1);
+    mbar_init(smem_u32(&ctrl->pv_taken), 1);
     mbar_init(smem_u32(&ctrl->hb[0]), kRowWarps / 2);
     mbar_init(smem_u32(&ctrl->hb[1]), kRowWarps / 2);
-    mbar_init(smem_u32(&ctrl->drain), role_s ? 2 : 1);  // S CTA: one commit per QK issuer
+    mbar_init(smem_u32(&ctrl->drain), role_s ? kNS : 1);  // S CTA: one commit per QK issuer
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -644,12 +655,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = data;
     if (warp == 0) {
       if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, cid, partner, rank == 0);
-    } else if (warp == 1 || warp == 3) {
-      // Two QK issuers, warp 1 for even pages and warp 3 for odd pages: one
-      // issuing thread sustains only about one N = 64 MMA per 55 cycles,
-      // two keep the tensor pipe full (32 cycles per MMA).
+    } else if (warp >= 1 && warp <= kNS) {
+      // kNS QK issuers (warps 1-3; warp 2 also owns the TMEM allocation):
+      // page j is issued by warp 1 + j % kNS into S buffer j % kNS.  One
+      // issuing thread sustains only about one N = 64 MMA per 55 cycles (and
+      // fewer while softmax warps share its scheduler); the tensor pipe
+      // takes one per 32 cycles.
       if (lane == 0) {
-        const uint32_t mine = warp == 1 ? 0u : 1u;
+        const uint32_t mine = static_cast<uint32_t>(warp - 1);
         UnitIter it;
         it.init(p, cid);
         Unit u;
@@ -661,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // issuer, and only those units are awaited: a unit without one is
           // skipped (its queries are never read here)
           const uint32_t npg = static_cast<uint32_t>(u.p1 - u.p0);
-          if (npg < 2 && (j & 1u) != mine) {
+          if (npg < static_cast<uint32_t>(kNS) && (mine + kNS - j % kNS) % kNS >= npg) {
             j += npg;
             continue;
           }
@@ -672,15 +685,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++qn;
           for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
-            if ((j & 1u) != mine) continue;
+            if (j % kNS != mine) continue;
             const int st = j % C::kNStS;
             const int sb = j % kNS;
             const uint32_t kph = (j / C::kNStS) & 1;
+            MLA_TRACE_POINT(0, 9, j);
             if (!mbar_wait(smem_u32(&ctrl->s_empty[sb]), ((j / kNS) & 1) ^ 1, abort, p.timeout_ns)) {
               ok = false;
               why = kWaitSEmpty;
               break;
             }
+            MLA_TRACE_POINT(0, 10, j);
             // descriptors of box 0 / the k_pe box at K step 0; a K step adds
             // 32 bytes (2 in the >>4 address field), a box adds 8 KB (512)
             const uint32_t slot_addr = smem_u32(ring + st * C::kSlotS);
@@ -773,12 +788,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float qs = 1.f;
         if (gg == 0) {
           // the queries of this unit replace the previous unit's in TMEM once
-          // every QK of that unit is done: the S of its last two pages (one
+          // every QK of that unit is done: the S of its last kNS pages (one
           // per issuer) has landed
-          for (uint32_t back = 1; back <= 2 && ok; ++back) {
+          for (uint32_t back = 1; back <= static_cast<uint32_t>(kNS) && ok; ++back) {
             if (j < back) break;
             const uint32_t jb = j - back;
-            if (!mbar_wait_warp(smem_u32(&ctrl->s_full[jb % kNS]), (jb / kNS) & 1, abort, p.timeout_ns)) {
+            if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->s_full[jb % kNS]), (jb / kNS) & 1, abort, p.timeout_ns)) {
               ok = false;
               why = kWaitSPrevUnit;
             }
@@ -788,8 +803,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           // release the queries to the QK issuer(s) of this unit's pages
-          if (lane == 0 && (npg >= 2 || (j & 1u) == 0)) mbar_arrive(smem_u32(&ctrl->q_full[0]));
-          if (lane == 0 && (npg >= 2 || (j & 1u) == 1)) mbar_arrive(smem_u32(&ctrl->q_full[1]));
+#pragma unroll
+          for (int m = 0; m < kNS; ++m)
+            if (lane == 0 && (npg >= kNS || (m + kNS - static_cast<int>(j % kNS)) % kNS < npg))
+              mbar_arrive(smem_u32(&ctrl->q_full[m]));
         } else if constexpr (kF8) {
           qs = query_scale(p, u.b, g, r);
         }
@@ -799,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
           if ((j & 1u) != static_cast<uint32_t>(gg)) continue;
           const int sb = j % kNS;
-          if (!mbar_wait_warp(smem_u32(&ctrl->s_full[sb]), (j / kNS) & 1, abort, p.timeout_ns)) {
+          if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->s_full[sb]), (j / kNS) & 1, abort, p.timeout_ns)) {
             ok = false;
             why = kWaitSFull;
             break;
@@ -836,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float m_prev = kMinusBig;
           if (j > 0) {
             const uint32_t jp = j - 1;
-            if (!mbar_wait_warp(smem_u32(&ctrl->hb[jp & 1]), (jp >> 1) & 1, abort, p.timeout_ns)) {
+            if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->hb[jp & 1]), (jp >> 1) & 1, abort, p.timeout_ns)) {
               ok = false;
               why = kWaitHandoff;
               break;
@@ -858,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P slot ps_slot is free once the O CTA finished PV of page j - ps.n
           const int ps_slot = static_cast<int>(j % static_cast<uint32_t>(ps.n));
           const uint32_t ps_phase = (j / static_cast<uint32_t>(ps.n)) & 1;
-          if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[ps_slot]), ps_phase ^ 1, abort, p.timeout_ns)) {
+          if (!mbar_wait_warp<true, true>(smem_u32(&ctrl->p_empty[ps_slot]), ps_phase ^ 1, abort, p.timeout_ns)) {
             ok = false;
             why = kWaitPEmptyS;
             break;
@@ -869,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // bytes on its p_full barrier; then the row's alpha
           const float nm = SoftmaxCfg<kF8>::kShift - m_ref;  // P = 2^(s * c2 - m_ref + shift)
           const uint32_t bar = mapa(smem_u32(&ctrl->p_full[ps_slot]), partner);
-          const uint32_t prow = p_remote + ps_slot * ps.stride + r * C::kPRow;
+          const uint32_t prow = p_remote + ps_slot * ps.stride + (r >> 3) * C::kPSbo + (r & 7) * 16;
           auto prob = [&](int t) {
             const float e = ex2_approx(fmaf(MLA_S(t), c2, nm));
             return (full || t0 + t < nvis) ? e : 0.f;
@@ -886,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
                 w[k] = *reinterpret_cast<uint32_t*>(&b2);
               }
-              if (real) st_async_v4(prow + ((c ^ (r & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]), bar);
+              if (real) st_async_v4(prow + c * C::kPLbo, make_uint4(w[0], w[1], w[2], w[3]), bar);
             }
           } else {
 #pragma unroll
@@ -907,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s4[k] += (fl.x + fl.y) + (fh.x + fh.y);
                 w[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
               }
-              if (real) st_async_v4(prow + ((c ^ ((r >> 1) & 3)) << 4), make_uint4(w[0], w[1], w[2], w[3]), bar);
+              if (real) st_async_v4(prow + c * C::kPLbo, make_uint4(w[0], w[1], w[2], w[3]), bar);
             }
           }
 #undef MLA_S
@@ -917,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // hand this group's (frame, partial sum) of the row to the O CTA
-        if (!mbar_wait_warp(smem_u32(&ctrl->ml_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
+        if (!mbar_wait_warp<true, true>(smem_u32(&ctrl->ml_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
           ok = false;
           why = kWaitMlEmpty;
           break;
@@ -939,14 +956,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const PSlots ps(kF8, rows_real);
     if (warp == 0) {
       if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, cid, partner, false);
-    } else if (warp == 1) {
+    } else if (warp == 3) {
+      // ---- waiter: gets page j ready for PV (c_kv landed, tail rows zeroed,
+      // P arrived, O free and rescaled) while the MMA warp issues PV(j - 1);
+      // the MMA warp then waits on one barrier per page
+      static_assert(C::kPartsO == 1, "the O ring holds whole pages");
       UnitIter it;
       it.init(p, cid);
       Unit u;
       uint32_t j = 0, un = 0;
       bool ok = true;
       int why = 0;
-      const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << partner));
       // the S CTA sends the P rows (and alphas) of real query rows only
       const uint32_t ptx = static_cast<uint32_t>(rows_real) * C::kPTxRow;
       if (lane == 0) {  // arm the P barriers of the first pages (bytes may land before or after)
@@ -959,92 +979,92 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
           const uint32_t pph = (j / static_cast<uint32_t>(ps.n)) & 1;
           uint8_t* slot = ring + st * C::kSlotO;
-          const int valid = u.L - pg * kPage;
-          // waits for ring part `part` of this page; token rows past the
-          // sequence end may hold anything (even NaN): they are zeroed so
-          // that P = 0 there cannot turn into 0 * NaN
-          auto part_ready = [&](int part) -> bool {
-            if (!mbar_wait_warp(smem_u32(&ctrl->kv_full[st * C::kPartsO + part]), kph, abort, p.timeout_ns))
-              return false;
-            if (valid < kPage) {
-              const int v0 = valid > 0 ? valid : 0;
-              const int nrows = kPage - v0;
-              for (int idx = lane; idx < C::kBoxesPartO * nrows * 8; idx += 32) {
-                const int chunk = idx & 7;
-                const int rowi = (idx >> 3) % nrows + v0;
-                const int box = part * C::kBoxesPartO + (idx >> 3) / nrows;
-                *reinterpret_cast<uint4*>(slot + box * C::kBox + rowi * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-              }
-              fence_proxy_async_cta();
-              __syncwarp();
-            }
-            return true;
-          };
-          if (!part_ready(0)) {
-            ok = false;
-            why = kWaitKvFullO;
-            break;
-          }
-          if (lane == 0) MLA_TRACE_POINT(1, 1, j);
-          if (!mbar_wait_warp(smem_u32(&ctrl->p_full[pb]), pph, abort, p.timeout_ns)) {
-            ok = false;
-            why = kWaitPFullO;
-            break;
-          }
-          // phase for page j done: arm this P slot for page j + ps.n.  Its
-          // bytes cannot come earlier: the S CTA sends them only after PV(j)
-          // ended.
-          if (lane == 0) mbar_expect_tx(smem_u32(&ctrl->p_full[pb]), ptx);
-          if (lane == 0) MLA_TRACE_POINT(1, 2, j);
+          if (lane == 0) MLA_TRACE_POINT(1, 8, j);
           const bool first = pg == u.p0;
           if (first && !mbar_wait_warp(smem_u32(&ctrl->o_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
             ok = false;
             why = kWaitOEmpty;
             break;
           }
-          if (!mbar_wait_warp(smem_u32(&ctrl->resc_done[pb]), pph, abort, p.timeout_ns)) {
-            ok = false;
-            why = kWaitRescDone;
-            break;
+          {  // PV(j - 1) taken, c_kv landed, P arrived, rescale acknowledged
+            const uint32_t bars[4] = {j > 0 ? smem_u32(&ctrl->pv_taken) : 0u, smem_u32(&ctrl->kv_full[st]),
+                                      smem_u32(&ctrl->p_full[pb]), smem_u32(&ctrl->resc_done[pb])};
+            const uint32_t pars[4] = {(j - 1) & 1, kph, pph, pph};
+            if (!mbar_wait4_warp(bars, pars, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitPFullO;
+              break;
+            }
           }
-          fence_proxy_async_cta();
-          tc_fence_after();
-          const uint64_t dp = smem_desc(smem_u32(pbuf + pb * ps.stride), 16, C::kPSbo, C::kPSwz);
-          const uint64_t dv = smem_desc(smem_u32(slot), C::kBox, 1024, kSwizzle128B);
-          // O[:, 256h .. 256h + 255] += P V[:, 256h ..]: one N half after the other,
-          // so the first c_kv part is consumed (and released) first
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (h > 0 && C::kPartsO > 1) {
-              if (!part_ready(1)) {
-                ok = false;
-                why = kWaitKvFullO;
-                break;
-              }
-              tc_fence_after();
+          // phase for page j done: arm this P slot for page j + ps.n.  Its
+          // bytes cannot come earlier: the S CTA sends them only after PV(j)
+          // ended.
+          if (lane == 0) mbar_expect_tx(smem_u32(&ctrl->p_full[pb]), ptx);
+          if (lane == 0) MLA_TRACE_POINT(1, 1, j);
+          const int valid = u.L - pg * kPage;
+          if (valid < kPage) {
+            // token rows past the sequence end may hold anything (even NaN):
+            // zero them so that P = 0 there cannot turn into 0 * NaN
+            const int v0 = valid > 0 ? valid : 0;
+            const int nrows = kPage - v0;
+            for (int idx = lane; idx < C::kBoxesPartO * nrows * 8; idx += 32) {
+              const int chunk = idx & 7;
+              const int rowi = (idx >> 3) % nrows + v0;
+              const int box = (idx >> 3) / nrows;
+              *reinterpret_cast<uint4*>(slot + box * C::kBox + rowi * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
             }
-            if (lane == 0) {
-#pragma unroll
-              for (int k = 0; k < C::kPvKSteps; ++k)
-                mma_ss<kF8>(tmem + h * 256, dp + static_cast<uint64_t>(k * 2),
-                            dv + static_cast<uint64_t>((h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes) >> 4),
-                            C::kIdescPV, (first && k == 0) ? 0u : 1u);
-              if (C::kPartsO > 1) mma_commit(smem_u32(&ctrl->kv_empty[st * C::kPartsO + h]));
-            }
+            fence_proxy_async_cta();
             __syncwarp();
           }
-          if (!ok) break;
+          if (lane == 0) MLA_TRACE_POINT(1, 2, j);
+          if (lane == 0) MLA_TRACE_POINT(1, 9, j);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->pv_ready));
+        }
+        ++un;
+      }
+      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
+    } else if (warp == 1) {
+      // ---- PV issuer
+      UnitIter it;
+      it.init(p, cid);
+      Unit u;
+      uint32_t j = 0;
+      bool ok = true;
+      const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << partner));
+      while (ok && it.next(u)) {
+        for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+          if (!mbar_wait_warp(smem_u32(&ctrl->pv_ready), j & 1, abort, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->pv_taken));
+          if (lane == 0) MLA_TRACE_POINT(1, 10, j);
+          const int st = j % C::kNStO;
+          const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
+          const bool first = pg == u.p0;
+          fence_proxy_async_cta();
+          tc_fence_after();
           if (lane == 0) {
-            if (C::kPartsO == 1) mma_commit(smem_u32(&ctrl->kv_empty[st]));
+            const uint64_t dp = smem_desc(smem_u32(pbuf + pb * ps.stride), C::kPLbo, C::kPSbo, C::kPSwz);
+            const uint64_t dv = smem_desc(smem_u32(ring + st * C::kSlotO), C::kBox, 1024, kSwizzle128B);
+            // O[:, 256h .. 256h + 255] += P V[:, 256h ..]
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int k = 0; k < C::kPvKSteps; ++k)
+                mma_ss<kF8>(tmem + h * 256, dp + static_cast<uint64_t>(k * (2 * C::kPLbo >> 4)),
+                            dv + static_cast<uint64_t>((h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes) >> 4),
+                            C::kIdescPV, (first && k == 0) ? 0u : 1u);
+            mma_commit(smem_u32(&ctrl->kv_empty[st]));
             mma_commit_multicast(smem_u32(&ctrl->p_empty[pb]), mask);
             if (pg == u.p1 - 1) mma_commit(smem_u32(&ctrl->o_full));
             MLA_TRACE_POINT(1, 3, j);
           }
           __syncwarp();
         }
-        ++un;
       }
-      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
+      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, kWaitPvReady, j);
       if (lane == 0) {
         mma_commit(smem_u32(&ctrl->drain));
         const uint64_t t0 = globaltimer_ns();
@@ -1072,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && it.next(u)) {
         for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
           const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
-          if (!mbar_wait_warp(smem_u32(&ctrl->p_full[pb]), (j / static_cast<uint32_t>(ps.n)) & 1, abort,
+          if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->p_full[pb]), (j / static_cast<uint32_t>(ps.n)) & 1, abort,
                               p.timeout_ns)) {
             ok = false;
             why = kWaitPFullCorr;
@@ -1085,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // wait until PV of the previous page has landed in O, then rescale
             const uint32_t jp = j - 1;
             const uint32_t np = static_cast<uint32_t>(ps.n);
-            if (!mbar_wait_warp(smem_u32(&ctrl->p_empty[jp % np]), (jp / np) & 1, abort, p.timeout_ns)) {
+            if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->p_empty[jp % np]), (jp / np) & 1, abort, p.timeout_ns)) {
               ok = false;
               why = kWaitPvPrev;
               break;
@@ -1109,12 +1129,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // epilogue for this unit
-        if (!mbar_wait_warp(smem_u32(&ctrl->o_full), un & 1, abort, p.timeout_ns)) {
+        if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->o_full), un & 1, abort, p.timeout_ns)) {
           ok = false;
           why = kWaitOFull;
           break;
         }
-        if (!mbar_wait_warp(smem_u32(&ctrl->ml_full), un & 1, abort, p.timeout_ns)) {
+        if (!mbar_wait_warp<true, true>(smem_u32(&ctrl->ml_full), un & 1, abort, p.timeout_ns)) {
           ok = false;
           why = kWaitMlFull;
           break;

@@ -104,16 +104,30 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 
 // Non-blocking test of a barrier phase (never suspends the thread: a
-// suspended waiter was measured to wake up hundreds of ns late).
+// suspended waiter was measured to wake up hundreds of ns late).  The
+// acquire is CTA-scoped by default: a cluster-scoped acquire was measured
+// to cost ~190 ns even on a completed phase, so it is used only where the
+// waiter then touches data the partner CTA wrote or will overwrite.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
@@ -121,28 +135,64 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // false when the wait gave up: after `limit_ns` of wall time, or at once if
 // *abort (a shared flag another thread set after its own wait gave up) is
 // non-zero.  The caller then records MLA_DEV_TIMEOUT and unwinds; nothing
-// ever spins without a limit.
+// ever spins without a limit.  With kBackoff the poller sleeps ~64 ns
+// between polls after a few quick ones: a spinning warp takes issue slots
+// from the warps sharing its scheduler (the MMA and TMA issuers).
+template <bool kCluster = false, bool kBackoff = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
 #pragma unroll 1
-  for (int i = 0; i < 64; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  for (int i = 0; i < (kBackoff ? 4 : 64); ++i)
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 16; ++i) {
+      if (mbar_try_wait<kCluster>(bar, parity)) return true;
+      if constexpr (kBackoff) __nanosleep(64);
+    }
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
+// Bounded wait for up to four barrier phases at once: each round tests all
+// pending ones back to back, so the polls' latencies overlap (sequential
+// waits on phases that are already complete each pay the full latency).
+// A bar of 0 is skipped.  Warp-wide, like mbar_wait_warp.
+__device__ __forceinline__ bool mbar_wait4_warp(const uint32_t (&bar)[4], const uint32_t (&parity)[4],
+                                                volatile int* abort, uint64_t limit_ns) {
+  uint32_t pending = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (bar[i]) pending |= 1u << i;
+  uint64_t t0 = 0;
+  bool ok = true;
+#pragma unroll 1
+  for (int round = 0; pending; ++round) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if ((pending >> i) & 1u)
+        if (mbar_try_wait(bar[i], parity[i])) pending &= ~(1u << i);
+    if (!pending) break;
+    if (round == 8) t0 = globaltimer_ns();
+    if (round > 8 && (round & 15) == 0) {
+      if (*abort || globaltimer_ns() - t0 > limit_ns) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Warp-wide bounded wait: every lane waits, and the warp agrees on the
 // outcome, so a timeout seen by one lane never splits the warp before a
 // .sync.aligned tcgen05 op or a vote.
+template <bool kCluster = false, bool kBackoff = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
                                                uint64_t limit_ns) {
-  const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+  const bool ok = mbar_wait<kCluster, kBackoff>(bar, parity, abort, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
