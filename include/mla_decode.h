@@ -90,8 +90,8 @@ size_t mla_decode_workspace_size(const mla_dims* d, int device);
  * One decode step: three kernels on `stream` (schedule, split-KV attention,
  * log-sum-exp combine).
  *
- *   q_nope      bf16 [B][q_len][H][512], contiguous, 16-byte aligned
- *   q_pe        bf16 [B][q_len][H][64],  contiguous, 16-byte aligned
+ *   q_nope      bf16 [B][q_len][H][512], contiguous, 32-byte aligned
+ *   q_pe        bf16 [B][q_len][H][64],  contiguous, 32-byte aligned
  *   kv_cache    bf16 or e4m3 [num_pages][64][576]: per token [c_kv | k_pe];
  *               an e4m3 value means code * kv_scale; 16-byte aligned
  *   page_table  int32 [B][page_table_stride]; entries beyond a request's
@@ -101,7 +101,8 @@ size_t mla_decode_workspace_size(const mla_dims* d, int device);
  *   q_len       must equal d->q_len
  *   scale       softmax scale applied to the whole score (e.g. 1/sqrt(192)); > 0
  *   kv_scale    per-tensor dequantisation scale of an e4m3 cache, > 0 (ignored for bf16)
- *   out         bf16 [B][q_len][H][512], 16-byte aligned
+ *   out         bf16 [B][q_len][H][512], 32-byte aligned (rows are read and written
+ *               32 bytes per access)
  *   lse         fp32 [B][q_len][H], natural log of sum exp(score)
  *   workspace   >= mla_decode_workspace_size bytes, 256-byte aligned device memory;
  *               holds the status words, the schedule and fp32 split partials;

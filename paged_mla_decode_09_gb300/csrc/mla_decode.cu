@@ -184,7 +184,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   // the softmax scale (and an e4m3 cache's scale) must be positive and finite
   if (!(scale > 0.f) || scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
   if (d->kv_dtype == MLA_KV_FP8_E4M3 && (!(kv_scale > 0.f) || kv_scale > 3.0e38f)) return MLA_ERR_INVALID_ARG;
-  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+  if (!aligned(q_nope, 32) || !aligned(q_pe, 32) || !aligned(kv_cache, 16) || !aligned(out, 32) ||
       !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
     return MLA_ERR_ALIGNMENT;
   int dev = 0;
@@ -431,7 +431,7 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   if (!q_nope || !q_pe || !kv_cache || !page_table || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
   if (d->kv_dtype == MLA_KV_FP8_E4M3 && (!(kv_scale > 0.f) || kv_scale > 3.0e38f)) return MLA_ERR_INVALID_ARG;
-  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+  if (!aligned(q_nope, 32) || !aligned(q_pe, 32) || !aligned(kv_cache, 16) || !aligned(out, 32) ||
       !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
       (status_out && !aligned(status_out, 4)))
     return MLA_ERR_ALIGNMENT;
@@ -513,6 +513,13 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
 
 #ifdef MLA_TRACE
 // Trace builds only: copies the event stamps of cluster 0 to host memory.
+extern "C" int mla_trace_set_cluster(int cid) {
+  return cudaMemcpyToSymbol(mla::g_mla_trace_cid, &cid, sizeof(int)) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+extern "C" int mla_trace_cluster_times(void* host_dst, size_t bytes) {
+  if (bytes > sizeof(mla::g_mla_cluster_times)) bytes = sizeof(mla::g_mla_cluster_times);
+  return cudaMemcpyFromSymbol(host_dst, mla::g_mla_cluster_times, bytes) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
 extern "C" int mla_trace_copy(void* host_dst, size_t bytes) {
   if (bytes > sizeof(mla::g_mla_trace)) bytes = sizeof(mla::g_mla_trace);
   return cudaMemcpyFromSymbol(host_dst, mla::g_mla_trace, bytes) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

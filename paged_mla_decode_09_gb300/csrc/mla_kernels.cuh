@@ -55,6 +55,10 @@ constexpr int kNS = 3;         // S accumulators in TMEM (S CTA)
 constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..287)
 constexpr int kCtrlBytes = 512;
 constexpr int kPrefetchAhead = 6;  // pages pulled into L2 ahead of the page the producer copies
+// Schedule weight of starting a request piece, in pages: a cluster pays a
+// fixed cost per piece it starts (queries into TMEM, pipeline refill,
+// epilogue), measured on GB300 at about the time of 8 to 12 pages.
+constexpr int kUnitCostPages = 10;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy output rescale: O is rescaled only when a row's running max grows by
@@ -198,9 +202,13 @@ struct Params {
 // of each pipeline event per page for cluster 0, for latency analysis.
 #ifdef MLA_TRACE
 __device__ uint64_t g_mla_trace[2][16][1024];
-#define MLA_TRACE_POINT(role, ev, j)                                                    \
-  do {                                                                                  \
-    if (cluster_id_x() == 0 && (j) < 1024) g_mla_trace[(role)][(ev)][(j)] = globaltimer_ns(); \
+// per cluster: [0] start, [1] S producer done, [2] O epilogue of the last unit done
+__device__ uint64_t g_mla_cluster_times[1024][4];
+__device__ int g_mla_trace_cid;  // the cluster whose events are stamped
+#define MLA_TRACE_POINT(role, ev, j)                                                                     \
+  do {                                                                                                   \
+    if (cluster_id_x() == static_cast<uint32_t>(g_mla_trace_cid) && (j) < 1024)                         \
+      g_mla_trace[(role)][(ev)][(j)] = globaltimer_ns();                                                 \
   } while (0)
 #else
 #define MLA_TRACE_POINT(role, ev, j) \
@@ -253,10 +261,26 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   }
   if (tid == 0) p.prefix[0] = 0;
   __syncthreads();
+  // Cluster slices are cut in a weighted order: request b occupies
+  // kUnitCostPages start-up units and then its pages, so clusters whose
+  // slice starts many pieces get fewer pages.  A weighted position maps to
+  // the page at that point (start-up units map to the request's first page).
   const int64_t T = p.prefix[p.B];
+  const int64_t W = T + static_cast<int64_t>(kUnitCostPages) * p.B;
+  auto page_at = [&](int64_t x) -> int {
+    int lo = 0, hi = p.B - 1;  // last request b with prefix[b] + kUnitCostPages * b <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.prefix[mid] + static_cast<int64_t>(kUnitCostPages) * mid <= x) lo = mid; else hi = mid - 1;
+    }
+    const int64_t np = p.prefix[lo + 1] - p.prefix[lo];
+    int64_t off = x - p.prefix[lo] - static_cast<int64_t>(kUnitCostPages) * lo - kUnitCostPages;
+    off = off < 0 ? 0 : (off > np ? np : off);
+    return static_cast<int>(p.prefix[lo] + off);
+  };
   for (int c = tid; c < p.C; c += 1024) {
-    const int s = static_cast<int>(T * c / p.C);
-    const int e = static_cast<int>(T * (c + 1) / p.C);
+    const int s = page_at(W * c / p.C);
+    const int e = page_at(W * (c + 1) / p.C);
     int lo = 0, hi = p.B - 1;  // last request b with prefix[b] <= s
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -389,7 +413,30 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
   PageCursor ahead;
   ahead.init(p, cid);
   uint32_t pf = 0;
+  // the queries of the unit after the current one are pulled into L2 too
+  // (the softmax loads them into TMEM at the unit boundary)
+  UnitIter nxt;
+  nxt.init(p, cid);
+  Unit un_next;
+  bool have_next = kRoleS && nxt.next(un_next);
+  if (have_next) {  // the first unit's queries, which the softmax loads right away
+    const int g = static_cast<int>(cluster_ctarank() >> 1);
+    const int rows = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
+    const int64_t row0 = static_cast<int64_t>(un_next.b) * p.Q * p.H + g * kRows;
+    prefetch_l2_bulk(p.q_nope + row0 * kDL * 2, static_cast<uint32_t>(rows) * kDL * 2);
+    prefetch_l2_bulk(p.q_pe + row0 * kDR * 2, static_cast<uint32_t>(rows) * kDR * 2);
+  }
   while (ok && it.next(u)) {
+    if (kRoleS) {  // every S CTA: its own row block's query rows
+      have_next = have_next && nxt.next(un_next);
+      if (have_next) {
+        const int g = static_cast<int>(cluster_ctarank() >> 1);
+        const int rows = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
+        const int64_t row0 = static_cast<int64_t>(un_next.b) * p.Q * p.H + g * kRows;
+        prefetch_l2_bulk(p.q_nope + row0 * kDL * 2, static_cast<uint32_t>(rows) * kDL * 2);
+        prefetch_l2_bulk(p.q_pe + row0 * kDR * 2, static_cast<uint32_t>(rows) * kDR * 2);
+      }
+    }
     for (int pg = u.p0; pg < u.p1 && ok; ++pg, ++j) {
       if (prefetch) {
         int pb, ppg;
@@ -454,35 +501,48 @@ __device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g,
     const int i = rr / p.H, h = rr % p.H;
     const int64_t orow = (static_cast<int64_t>(u.b) * p.Q + i) * p.H + h;
     uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDL * 2);
-    for (int c = half * 256; c < half * 256 + 256; c += 16) {
-      uint32_t v[16];
-      tmem_ld16(taddr_row + c, v);
-      tmem_wait_ld_tie(v);
+#pragma unroll 1
+    for (int c = half * 256; c < half * 256 + 256; c += 32) {  // two TMEM loads in flight per wait
+      uint32_t v[2][16];
+      tmem_ld16(taddr_row + c, v[0]);
+      tmem_ld16(taddr_row + c + 16, v[1]);
+      tmem_wait_ld_tie(v[0]);
+      tmem_wait_ld_tie(v[1]);
       if (real) {
-        uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * k]) * oscale,
-                                                    __uint_as_float(v[2 * k + 1]) * oscale);
-          w[k] = *reinterpret_cast<uint32_t*>(&b2);
+        for (int q = 0; q < 2; ++q) {
+          uint32_t w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[q][2 * k]) * oscale,
+                                                      __uint_as_float(v[q][2 * k + 1]) * oscale);
+            w[k] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          stg_v8(dst + (c + 16 * q) / 8, w);  // 16 bf16 = 32 bytes
         }
-        dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
     }
     if (real && half == 0) p.lse[orow] = lse_v;
   } else {
     const int64_t prow = (static_cast<int64_t>(u.slot) * p.G + g) * kRows + r;
     float4* dst = reinterpret_cast<float4*>(p.o_part + prow * kDL);
-    for (int c = half * 256; c < half * 256 + 256; c += 16) {
-      uint32_t v[16];
-      tmem_ld16(taddr_row + c, v);
-      tmem_wait_ld_tie(v);
+#pragma unroll 1
+    for (int c = half * 256; c < half * 256 + 256; c += 32) {
+      uint32_t v[2][16];
+      tmem_ld16(taddr_row + c, v[0]);
+      tmem_ld16(taddr_row + c + 16, v[1]);
+      tmem_wait_ld_tie(v[0]);
+      tmem_wait_ld_tie(v[1]);
       if (real) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[c / 4 + k] = make_float4(__uint_as_float(v[4 * k]) * oscale, __uint_as_float(v[4 * k + 1]) * oscale,
-                                       __uint_as_float(v[4 * k + 2]) * oscale, __uint_as_float(v[4 * k + 3]) * oscale);
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(v[q][8 * k + e]) * oscale);
+            stg_v8(dst + (c + 16 * q) / 4 + 2 * k, w);  // 8 floats = 32 bytes
+          }
       }
     }
     if (real && half == 0) p.lse_part[prow] = lse_v;
@@ -490,10 +550,12 @@ __device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g,
 }
 
 // Loads query row r of row block g for request b into TMEM lane r (packed
-// along K: 2 bf16 or 4 e4m3 per column).  For e4m3 returns the row's
-// quantisation scale (value = code * scale).
-template <bool kF8>
-__device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r, uint32_t taddr_row) {
+// along K: 2 bf16 or 4 e4m3 per column).  bf16: only the 16-byte chunks
+// [c0, c0 + kN) of the row (chunk c = 8 values: c < 64 from q_nope, else
+// q_pe), 12 loads in flight per round.  e4m3 (whole row, kN ignored): returns
+// the row's quantisation scale (value = code * scale).
+template <bool kF8, int kN = 72>
+__device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r, uint32_t taddr_row, int c0 = 0) {
   const int rr = g * kRows + r;
   const bool real = rr < p.R;
   const uint4* qn = nullptr;
@@ -504,33 +566,49 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
     qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
     qp = reinterpret_cast<const uint4*>(p.q_pe + row * kDR * 2);
   }
-  // chunk c of 8 bf16 values (16 bytes), c in [0, 72)
-  auto chunk = [&](int c) -> uint4 {
-    if (!real) return make_uint4(0, 0, 0, 0);
-    return c < 64 ? __ldg(qn + c) : __ldg(qp + (c - 64));
+  // chunks c, c + 1 (c even; chunk = 8 bf16 values) as one 32-byte load
+  auto pair = [&](int c, uint32_t (&w)[8]) {
+    if (!real) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = 0u;
+    } else {
+      ldg_v8(c < 64 ? static_cast<const void*>(qn + c) : static_cast<const void*>(qp + (c - 64)), w);
+    }
   };
   if constexpr (!kF8) {
-    for (int c = 0; c < 72; c += 4) {
-      uint32_t w[16];
+    static_assert(kN % 12 == 0, "rounds of 12 chunks");
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 v = chunk(c + k);
-        w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+    for (int c = 0; c < kN; c += 12) {
+      uint32_t v[6][8];
+#pragma unroll
+      for (int k = 0; k < 6; ++k) pair(c0 + c + 2 * k, v[k]);
+#pragma unroll
+      for (int s4 = 0; s4 < 3; ++s4) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          w[e] = v[2 * s4][e];
+          w[8 + e] = v[2 * s4 + 1][e];
+        }
+        tmem_st16(taddr_row + (c0 + c + 4 * s4) * 4, w);
       }
-      tmem_st16(taddr_row + c * 4, w);
     }
     tmem_wait_st();
     return 1.f;
   } else {
     float amax = 0.f;
-    for (int c = 0; c < 72; ++c) {
-      const uint4 v = chunk(c);
-      const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll 1
+    for (int c = 0; c < 72; c += 12) {
+      uint32_t v[6][8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
+      for (int k = 0; k < 6; ++k) pair(c + 2 * k, v[k]);
+#pragma unroll
+      for (int k = 0; k < 6; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[k][e]));
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
     }
     const float qs = amax > 0.f ? amax / 448.f : 1.f;
     const float inv = 1.f / qs;
@@ -544,12 +622,16 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
       hi16 = h;
       lo16 = l;
     };
+#pragma unroll 1
     for (int c = 0; c < 72; c += 8) {  // 64 values -> 16 columns of each term
+      uint32_t v8[4][8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pair(c + 2 * k, v8[k]);
       uint32_t whi[16], wlo[16];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint4 v = chunk(c + k);
-        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t ws[4] = {v8[k >> 1][4 * (k & 1)], v8[k >> 1][4 * (k & 1) + 1], v8[k >> 1][4 * (k & 1) + 2],
+                                v8[k >> 1][4 * (k & 1) + 3]};
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[2 * h2]));
@@ -579,14 +661,21 @@ __device__ __forceinline__ float query_scale(const Params& p, int b, int g, int 
   const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
   const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + row * kDR * 2);
   float amax = 0.f;
-  for (int c = 0; c < 72; ++c) {
-    const uint4 v = c < 64 ? __ldg(qn + c) : __ldg(qp + (c - 64));
-    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll 1
+  for (int c = 0; c < 72; c += 12) {
+    uint32_t v[6][8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    for (int k = 0; k < 6; ++k) {
+      const int cc = c + 2 * k;
+      ldg_v8(cc < 64 ? static_cast<const void*>(qn + cc) : static_cast<const void*>(qp + (cc - 64)), v[k]);
     }
+#pragma unroll
+    for (int k = 0; k < 6; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[k][e]));
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
   }
   return amax > 0.f ? amax / 448.f : 1.f;
 }
@@ -617,7 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->s_full[i]), 1);
       mbar_init(smem_u32(&ctrl->s_empty[i]), kRowWarps / 2);  // the group that read the page
     }
-    for (int i = 0; i < kNS; ++i) mbar_init(smem_u32(&ctrl->q_full[i]), kRowWarps / 2);  // group 0 loads queries
+    // the warps that load the queries: both groups (bf16) or group 0 (e4m3)
+    for (int i = 0; i < kNS; ++i) mbar_init(smem_u32(&ctrl->q_full[i]), kF8 ? kRowWarps / 2 : kRowWarps);
     for (int i = 0; i < kMaxPSlots; ++i) {
       mbar_init(smem_u32(&ctrl->p_full[i]), 1);  // one arm (expect_tx) by the O MMA warp + P bytes
       mbar_init(smem_u32(&ctrl->p_empty[i]), 1);
@@ -649,6 +739,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // partner barriers initialised before any remote arrive
   const uint32_t tmem = ctrl->tmem_base;
   volatile int* abort = &ctrl->abort;
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0 && rank == 0 && cid < 1024) g_mla_cluster_times[cid][0] = globaltimer_ns();
+#endif
 
   if (role_s) {
     // =========================== S CTA ===========================
@@ -786,20 +879,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && it.next(u)) {
         const int npg = u.p1 - u.p0;
         float qs = 1.f;
-        if (gg == 0) {
+        // bf16: both groups load half of every query row; e4m3: group 0 loads
+        // whole rows (the per-row scale needs all of it), group 1 computes
+        // the scale alone
+        if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 11, un);
+        if (gg == 0 || !kF8) {
           // the queries of this unit replace the previous unit's in TMEM once
           // every QK of that unit is done: the S of its last kNS pages (one
           // per issuer) has landed
           for (uint32_t back = 1; back <= static_cast<uint32_t>(kNS) && ok; ++back) {
             if (j < back) break;
             const uint32_t jb = j - back;
-            if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->s_full[jb % kNS]), (jb / kNS) & 1, abort, p.timeout_ns)) {
+            if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->s_full[jb % kNS]), (jb / kNS) & 1, abort,
+                                             p.timeout_ns)) {
               ok = false;
               why = kWaitSPrevUnit;
             }
           }
           if (!ok) break;
-          qs = load_q_row<kF8>(p, u.b, g, r, tmem + lane_base);
+          if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 12, un);
+          if constexpr (kF8) {
+            qs = load_q_row<true>(p, u.b, g, r, tmem + lane_base);
+          } else {
+            load_q_row<false, 36>(p, u.b, g, r, tmem + lane_base, 36 * gg);
+          }
           tc_fence_before();
           __syncwarp();
           // release the queries to the QK issuer(s) of this unit's pages
@@ -807,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int m = 0; m < kNS; ++m)
             if (lane == 0 && (npg >= kNS || (m + kNS - static_cast<int>(j % kNS)) % kNS < npg))
               mbar_arrive(smem_u32(&ctrl->q_full[m]));
+          if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 13, un);
         } else if constexpr (kF8) {
           qs = query_scale(p, u.b, g, r);
         }
@@ -1129,11 +1233,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // epilogue for this unit
+        if (r == 0 && half == 0) MLA_TRACE_POINT(1, 13, un);
         if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->o_full), un & 1, abort, p.timeout_ns)) {
           ok = false;
           why = kWaitOFull;
           break;
         }
+        if (r == 0 && half == 0) MLA_TRACE_POINT(1, 14, un);
         if (!mbar_wait_warp<true, true>(smem_u32(&ctrl->ml_full), un & 1, abort, p.timeout_ns)) {
           ok = false;
           why = kWaitMlFull;
@@ -1165,6 +1271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0 && cid < 1024) g_mla_cluster_times[cid][1 + (rank & 1)] = globaltimer_ns();
+#endif
   if (warp == 2) tmem_dealloc(tmem, 512);
   cluster_sync();
 }
@@ -1172,9 +1281,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------- K2
 // Merges the fp32 partials of every request cut by a slice boundary:
 // lse = log sum_s exp(lse_s), out = sum_s exp(lse_s - lse) * out_s.
-__device__ __forceinline__ int slice_of(int64_t x, int64_t T, int C) {
-  return static_cast<int>(((x + 1) * C - 1) / T);
-}
 
 __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
   const int b = blockIdx.x, g = blockIdx.y;
@@ -1182,11 +1288,28 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
   const int r = blockIdx.z * 8 + warp;
   const int rr = g * kRows + r;
   if (rr >= p.R) return;
-  const int64_t T = p.prefix[p.B];
   const int pb0 = p.prefix[b], pb1 = p.prefix[b + 1];
   if (pb1 <= pb0) return;
-  const int clo = slice_of(pb0, T, p.C), chi = slice_of(pb1 - 1, T, p.C);
-  if (clo == chi) return;
+  // clusters whose slice [s, e) meets the request's pages [pb0, pb1): from
+  // the first with e > pb0 to the last with s < pb1 (both bounds are
+  // non-decreasing in the cluster index)
+  int clo = 0, chi = p.C - 1;
+  {
+    int lo = 0, hi = p.C - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (p.cinfo[3 * mid + 1] > pb0) hi = mid; else lo = mid + 1;
+    }
+    clo = lo;
+    lo = 0;
+    hi = p.C - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.cinfo[3 * mid] < pb1) lo = mid; else hi = mid - 1;
+    }
+    chi = lo;
+  }
+  if (clo >= chi) return;  // the whole request in one slice: written directly
   // slices strictly between clo and chi may be empty (fewer pages than
   // clusters): an empty slice holds no piece and is skipped
   float mx = -INFINITY;
