@@ -54,7 +54,9 @@ constexpr int kRowWarps = 8;  // row-warp barriers take one arrival per warp (la
 constexpr int kNS = 3;         // S accumulators in TMEM (S CTA)
 constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..287)
 constexpr int kCtrlBytes = 512;
-constexpr int kPrefetchAhead = 6;  // pages pulled into L2 ahead of the page the producer copies
+// The S CTA's producer pulls pages into L2 this many pages ahead of its
+// copies, so that a copy (issued when a ring slot frees up) reads L2.
+constexpr int kPrefetchAhead = 6;
 // Schedule weight of starting a request piece, in pages: a cluster pays a
 // fixed cost per piece it starts (queries into TMEM, pipeline refill,
 // epilogue), measured on GB300 at about the time of 8 to 12 pages.
@@ -162,7 +164,7 @@ struct __align__(8) Ctrl {
   uint64_t kv_empty[9];
   uint64_t s_full[kNS];
   uint64_t s_empty[kNS];
-  uint64_t q_full[kNS];  // queries of the unit loaded, per QK issuer (page j: issuer j % kNS)
+  uint64_t q_full;  // queries of the unit loaded into TMEM
   uint64_t p_full[kMaxPSlots];
   uint64_t p_empty[kMaxPSlots];
   uint64_t o_full;
@@ -389,7 +391,7 @@ __device__ __forceinline__ int32_t read_page_id(const Params& p, int b, int pg) 
 // of kNSt slots, each filled by kParts copies with their own barriers.
 template <bool kF8, bool kRoleS>
 __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const CUtensorMap* tm_kv,
-                             const CUtensorMap* tm_pe, int cid, uint32_t partner, bool prefetch) {
+                             const CUtensorMap* tm_pe, int cid, uint32_t partner, bool prefetch_pages) {
   using C = Cfg<kF8>;
   constexpr int kNSt = kRoleS ? C::kNStS : C::kNStO;
   constexpr int kSlot = kRoleS ? C::kSlotS : C::kSlotO;
@@ -408,8 +410,8 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
   // phase (i / kNQ) & 1
   constexpr uint32_t kNQ = kNSt * kParts;
   uint32_t copies = 0;
-  // Pages kNSt .. are pulled into L2 kPrefetchAhead pages before their copy
-  // is issued, so that the copy (issued when a ring slot frees up) reads L2.
+  // With prefetch_pages, pages are pulled into L2 kPrefetchAhead pages
+  // before this producer copies them.
   PageCursor ahead;
   ahead.init(p, cid);
   uint32_t pf = 0;
@@ -438,13 +440,11 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
       }
     }
     for (int pg = u.p0; pg < u.p1 && ok; ++pg, ++j) {
-      if (prefetch) {
+      if (prefetch_pages) {
         int pb, ppg;
         while (pf < j + kPrefetchAhead && ahead.next(pb, ppg)) {
-          if (pf >= static_cast<uint32_t>(kNSt)) {
-            const int32_t pid = __ldg(p.page_table + static_cast<int64_t>(pb) * p.pt_stride + ppg);
-            if (pid >= 0 && pid < p.num_pages) prefetch_l2_bulk(p.kv + static_cast<int64_t>(pid) * kPageBytes, kPageBytes);
-          }
+          const int32_t pid = __ldg(p.page_table + static_cast<int64_t>(pb) * p.pt_stride + ppg);
+          if (pid >= 0 && pid < p.num_pages) prefetch_l2_bulk(p.kv + static_cast<int64_t>(pid) * kPageBytes, kPageBytes);
           ++pf;
         }
       }
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->s_empty[i]), kRowWarps / 2);  // the group that read the page
     }
     // the warps that load the queries: both groups (bf16) or group 0 (e4m3)
-    for (int i = 0; i < kNS; ++i) mbar_init(smem_u32(&ctrl->q_full[i]), kF8 ? kRowWarps / 2 : kRowWarps);
+    mbar_init(smem_u32(&ctrl->q_full), kF8 ? kRowWarps / 2 : kRowWarps);
     for (int i = 0; i < kMaxPSlots; ++i) {
       mbar_init(smem_u32(&ctrl->p_full[i]), 1);  // one arm (expect_tx) by the O MMA warp + P bytes
       mbar_init(smem_u32(&ctrl->p_empty[i]), 1);
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&ctrl->pv_taken), 1);
     mbar_init(smem_u32(&ctrl->hb[0]), kRowWarps / 2);
     mbar_init(smem_u32(&ctrl->hb[1]), kRowWarps / 2);
-    mbar_init(smem_u32(&ctrl->drain), role_s ? kNS : 1);  // S CTA: one commit per QK issuer
+    mbar_init(smem_u32(&ctrl->drain), 1);
     ctrl->abort = 0;
     fence_barrier_init();
   }
@@ -748,111 +748,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ring = data;
     if (warp == 0) {
       if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, cid, partner, rank == 0);
-    } else if (warp >= 1 && warp <= kNS) {
-      // kNS QK issuers (warps 1-3; warp 2 also owns the TMEM allocation):
-      // page j is issued by warp 1 + j % kNS into S buffer j % kNS.  One
-      // issuing thread sustains only about one N = 64 MMA per 55 cycles (and
-      // fewer while softmax warps share its scheduler); the tensor pipe
-      // takes one per 32 cycles.
-      if (lane == 0) {
-        const uint32_t mine = static_cast<uint32_t>(warp - 1);
-        UnitIter it;
-        it.init(p, cid);
-        Unit u;
-        uint32_t j = 0, qn = 0;
-        bool ok = true;
-        int why = 0;
-        while (ok && it.next(u)) {
-          // q_full[mine] completes once per unit holding a page of this
-          // issuer, and only those units are awaited: a unit without one is
-          // skipped (its queries are never read here)
-          const uint32_t npg = static_cast<uint32_t>(u.p1 - u.p0);
-          if (npg < static_cast<uint32_t>(kNS) && (mine + kNS - j % kNS) % kNS >= npg) {
-            j += npg;
-            continue;
-          }
-          if (!mbar_wait(smem_u32(&ctrl->q_full[mine]), qn & 1, abort, p.timeout_ns)) {
+    } else if (warp == 1) {
+      // QK issuer: the whole warp runs the loop and one elected lane issues
+      // (a converged warp keeps the tensor pipe full with N = 64 MMAs), so
+      // each page's 36 MMAs run back to back and its ring slot frees early
+      UnitIter it;
+      it.init(p, cid);
+      Unit u;
+      uint32_t j = 0, un = 0;
+      bool ok = true;
+      int why = 0;
+      while (ok && it.next(u)) {
+        if (!mbar_wait_warp(smem_u32(&ctrl->q_full), un & 1, abort, p.timeout_ns)) {
+          ok = false;
+          why = kWaitQFull;
+          break;
+        }
+        ++un;
+        for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
+          const int st = j % C::kNStS;
+          const int sb = j % kNS;
+          const uint32_t kph = (j / C::kNStS) & 1;
+          if (lane == 0) MLA_TRACE_POINT(0, 9, j);
+          if (!mbar_wait_warp(smem_u32(&ctrl->s_empty[sb]), ((j / kNS) & 1) ^ 1, abort, p.timeout_ns)) {
             ok = false;
-            why = kWaitQFull;
+            why = kWaitSEmpty;
             break;
           }
-          ++qn;
-          for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
-            if (j % kNS != mine) continue;
-            const int st = j % C::kNStS;
-            const int sb = j % kNS;
-            const uint32_t kph = (j / C::kNStS) & 1;
-            MLA_TRACE_POINT(0, 9, j);
-            if (!mbar_wait(smem_u32(&ctrl->s_empty[sb]), ((j / kNS) & 1) ^ 1, abort, p.timeout_ns)) {
-              ok = false;
-              why = kWaitSEmpty;
-              break;
-            }
-            MLA_TRACE_POINT(0, 10, j);
-            // descriptors of box 0 / the k_pe box at K step 0; a K step adds
-            // 32 bytes (2 in the >>4 address field), a box adds 8 KB (512)
-            const uint32_t slot_addr = smem_u32(ring + st * C::kSlotS);
-            const uint64_t dlat = smem_desc(slot_addr, 16, 1024, kSwizzle128B);
-            const uint32_t dcol = tmem + kSCol0 + sb * 64;
-            if constexpr (!kF8) {
-              // 9 boxes (8 of c_kv, 1 of k_pe) x 4 K steps, part by part
-#pragma unroll
-              for (int part = 0; part < C::kPartsS; ++part) {
-                const int q = st * C::kPartsS + part;
-                if (!mbar_wait(smem_u32(&ctrl->kv_full[q]), kph, abort, p.timeout_ns)) {
-                  ok = false;
-                  why = kWaitKvFullS;
-                  break;
-                }
-                if (part == 0) MLA_TRACE_POINT(0, 1, j);
-                tc_fence_after();
-#pragma unroll
-                for (int dd = 0; dd < C::kBoxesPartS; ++dd) {
-                  const int d = part * C::kBoxesPartS + dd;
-#pragma unroll
-                  for (int k = 0; k < 4; ++k)
-                    mma_ts<false>(dcol, tmem + d * 32 + k * 8, dlat + static_cast<uint64_t>(d * 512 + k * 2),
-                                  C::kIdescQK, (d | k) ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&ctrl->kv_empty[q]));
-              }
-              if (!ok) break;
-            } else {
-              if (!mbar_wait(smem_u32(&ctrl->kv_full[st]), kph, abort, p.timeout_ns)) {
-                ok = false;
-                why = kWaitKvFullS;
-                break;
-              }
-              MLA_TRACE_POINT(0, 1, j);
-              tc_fence_after();
-              const uint64_t dpe = smem_desc(slot_addr + C::kNBoxLat * C::kBox, 16, C::kPeSbo, C::kPeSwz);
-#pragma unroll
-              for (int term = 0; term < C::kQSplit; ++term) {
-                const uint32_t qcol = tmem + (term ? C::kQLoCol : 0u);
-#pragma unroll
-                for (int d = 0; d < C::kNBoxLat; ++d) {
-#pragma unroll
-                  for (int k = 0; k < 4; ++k)
-                    mma_ts<true>(dcol, qcol + d * 32 + k * 8, dlat + static_cast<uint64_t>(d * 512 + k * 2),
-                                 C::kIdescQK, (term | d | k) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int k = 0; k < C::kKStepsPe; ++k)
-                  mma_ts<true>(dcol, qcol + C::kNBoxLat * 32 + k * 8, dpe + static_cast<uint64_t>(k * 2),
-                               C::kIdescQK, 1u);
-              }
-              mma_commit(smem_u32(&ctrl->kv_empty[st]));
-            }
-            mma_commit(smem_u32(&ctrl->s_full[sb]));
-            MLA_TRACE_POINT(0, 2, j);
+          if (!mbar_wait_warp(smem_u32(&ctrl->kv_full[st]), kph, abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitKvFullS;
+            break;
           }
+          if (lane == 0) MLA_TRACE_POINT(0, 1, j);
+          tc_fence_after();
+          // descriptors of box 0 / the k_pe box at K step 0; a K step adds
+          // 32 bytes (2 in the >>4 address field), a box adds 8 KB (512)
+          const uint32_t slot_addr = smem_u32(ring + st * C::kSlotS);
+          const uint64_t dlat = smem_desc(slot_addr, 16, 1024, kSwizzle128B);
+          const uint32_t dcol = tmem + kSCol0 + sb * 64;
+          if constexpr (!kF8) {
+            // 9 boxes (8 of c_kv, 1 of k_pe) x 4 K steps
+#pragma unroll
+            for (int d = 0; d < 9; ++d)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_ts_e<false>(dcol, tmem + d * 32 + k * 8, dlat + static_cast<uint64_t>(d * 512 + k * 2),
+                                C::kIdescQK, (d | k) ? 1u : 0u);
+          } else {
+            const uint64_t dpe = smem_desc(slot_addr + C::kNBoxLat * C::kBox, 16, C::kPeSbo, C::kPeSwz);
+#pragma unroll
+            for (int term = 0; term < C::kQSplit; ++term) {
+              const uint32_t qcol = tmem + (term ? C::kQLoCol : 0u);
+#pragma unroll
+              for (int d = 0; d < C::kNBoxLat; ++d)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mma_ts_e<true>(dcol, qcol + d * 32 + k * 8, dlat + static_cast<uint64_t>(d * 512 + k * 2),
+                                 C::kIdescQK, (term | d | k) ? 1u : 0u);
+#pragma unroll
+              for (int k = 0; k < C::kKStepsPe; ++k)
+                mma_ts_e<true>(dcol, qcol + C::kNBoxLat * 32 + k * 8, dpe + static_cast<uint64_t>(k * 2),
+                               C::kIdescQK, 1u);
+            }
+          }
+          mma_commit_e(smem_u32(&ctrl->kv_empty[st]));
+          mma_commit_e(smem_u32(&ctrl->s_full[sb]));
+          if (lane == 0) MLA_TRACE_POINT(0, 2, j);
         }
-        if (!ok) raise_timeout(p, ctrl, partner, why, j);
-        mma_commit(smem_u32(&ctrl->drain));
+      }
+      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
+      mma_commit_e(smem_u32(&ctrl->drain));
+      if (lane == 0) {
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(&ctrl->drain), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
         }
       }
+      __syncwarp();
     } else if (warp >= 4) {
       // ---- softmax: group gg (warps 4-7: 0, warps 8-11: 1) takes the pages
       // j with j % 2 == gg; its thread r owns query row r.  The running max
@@ -877,7 +849,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int why = 0;
       while (ok && it.next(u)) {
-        const int npg = u.p1 - u.p0;
         float qs = 1.f;
         // bf16: both groups load half of every query row; e4m3: group 0 loads
         // whole rows (the per-row scale needs all of it), group 1 computes
@@ -885,18 +856,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 11, un);
         if (gg == 0 || !kF8) {
           // the queries of this unit replace the previous unit's in TMEM once
-          // every QK of that unit is done: the S of its last kNS pages (one
-          // per issuer) has landed
-          for (uint32_t back = 1; back <= static_cast<uint32_t>(kNS) && ok; ++back) {
-            if (j < back) break;
-            const uint32_t jb = j - back;
-            if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->s_full[jb % kNS]), (jb / kNS) & 1, abort,
-                                             p.timeout_ns)) {
-              ok = false;
-              why = kWaitSPrevUnit;
-            }
+          // every QK of that unit is done: the S of its last page has landed
+          // (one issuer: its commit covers all its earlier MMAs)
+          if (j > 0 && !mbar_wait_warp<false, true>(smem_u32(&ctrl->s_full[(j - 1) % kNS]), ((j - 1) / kNS) & 1,
+                                                    abort, p.timeout_ns)) {
+            ok = false;
+            why = kWaitSPrevUnit;
+            break;
           }
-          if (!ok) break;
           if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 12, un);
           if constexpr (kF8) {
             qs = load_q_row<true>(p, u.b, g, r, tmem + lane_base);
@@ -905,11 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           __syncwarp();
-          // release the queries to the QK issuer(s) of this unit's pages
-#pragma unroll
-          for (int m = 0; m < kNS; ++m)
-            if (lane == 0 && (npg >= kNS || (m + kNS - static_cast<int>(j % kNS)) % kNS < npg))
-              mbar_arrive(smem_u32(&ctrl->q_full[m]));
+          // release the queries to the QK issuer
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->q_full));
           if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 13, un);
         } else if constexpr (kF8) {
           qs = query_scale(p, u.b, g, r);
@@ -1149,7 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool first = pg == u.p0;
           fence_proxy_async_cta();
           tc_fence_after();
-          if (lane == 0) {
+          {  // the whole warp issues; one elected lane executes
             const uint64_t dp = smem_desc(smem_u32(pbuf + pb * ps.stride), C::kPLbo, C::kPSbo, C::kPSwz);
             const uint64_t dv = smem_desc(smem_u32(ring + st * C::kSlotO), C::kBox, 1024, kSwizzle128B);
             // O[:, 256h .. 256h + 255] += P V[:, 256h ..]
@@ -1157,20 +1121,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int k = 0; k < C::kPvKSteps; ++k)
-                mma_ss<kF8>(tmem + h * 256, dp + static_cast<uint64_t>(k * (2 * C::kPLbo >> 4)),
-                            dv + static_cast<uint64_t>((h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes) >> 4),
-                            C::kIdescPV, (first && k == 0) ? 0u : 1u);
-            mma_commit(smem_u32(&ctrl->kv_empty[st]));
-            mma_commit_multicast(smem_u32(&ctrl->p_empty[pb]), mask);
-            if (pg == u.p1 - 1) mma_commit(smem_u32(&ctrl->o_full));
-            MLA_TRACE_POINT(1, 3, j);
+                mma_ss_e<kF8>(tmem + h * 256, dp + static_cast<uint64_t>(k * (2 * C::kPLbo >> 4)),
+                              dv + static_cast<uint64_t>((h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes) >> 4),
+                              C::kIdescPV, (first && k == 0) ? 0u : 1u);
+            mma_commit_e(smem_u32(&ctrl->kv_empty[st]));
+            mma_commit_multicast_e(smem_u32(&ctrl->p_empty[pb]), mask);
+            if (pg == u.p1 - 1) mma_commit_e(smem_u32(&ctrl->o_full));
+            if (lane == 0) MLA_TRACE_POINT(1, 3, j);
           }
-          __syncwarp();
         }
       }
       if (!ok && lane == 0) raise_timeout(p, ctrl, partner, kWaitPvReady, j);
+      mma_commit_e(smem_u32(&ctrl->drain));
       if (lane == 0) {
-        mma_commit(smem_u32(&ctrl->drain));
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(&ctrl->drain), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
         }
