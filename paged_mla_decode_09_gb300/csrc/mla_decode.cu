@@ -202,7 +202,6 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Params p;
-  p.kv = static_cast<const uint8_t*>(kv_cache);
   p.q_nope = static_cast<const uint8_t*>(q_nope);
   p.q_pe = static_cast<const uint8_t*>(q_pe);
   p.page_table = page_table;
@@ -454,7 +453,6 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
 
   Params p;
-  p.kv = static_cast<const uint8_t*>(kv_cache);
   p.q_nope = static_cast<const uint8_t*>(q_nope);
   p.q_pe = static_cast<const uint8_t*>(q_pe);
   p.page_table = page_table;

@@ -54,9 +54,6 @@ constexpr int kRowWarps = 8;  // row-warp barriers take one arrival per warp (la
 constexpr int kNS = 3;         // S accumulators in TMEM (S CTA)
 constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..287)
 constexpr int kCtrlBytes = 512;
-// The S CTA's producer pulls pages into L2 this many pages ahead of its
-// copies, so that a copy (issued when a ring slot frees up) reads L2.
-constexpr int kPrefetchAhead = 6;
 // Schedule weight of starting a request piece, in pages: a cluster pays a
 // fixed cost per piece it starts (queries into TMEM, pipeline refill,
 // epilogue), measured on GB300 at about the time of 8 to 12 pages.
@@ -182,7 +179,6 @@ struct __align__(8) Ctrl {
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 struct Params {
-  const uint8_t* kv;       // cache pool (read only by the L2 prefetch; pages come by TMA)
   const uint8_t* q_nope;   // bf16
   const uint8_t* q_pe;     // bf16
   const int32_t* page_table;
@@ -336,29 +332,6 @@ struct UnitIter {
   }
 };
 
-// The slice's pages in processing order, one at a time.
-struct PageCursor {
-  UnitIter it;
-  Unit u;
-  int pg;
-  bool live;
-  __device__ void init(const Params& p, int c) {
-    it.init(p, c);
-    live = it.next(u);
-    pg = live ? u.p0 : 0;
-  }
-  __device__ bool next(int& b, int& page) {
-    while (live && pg >= u.p1) {
-      live = it.next(u);
-      if (live) pg = u.p0;
-    }
-    if (!live) return false;
-    b = u.b;
-    page = pg++;
-    return true;
-  }
-};
-
 // Which wait gave up, recorded (first one only) in status[1..3] of the
 // workspace: wait tag, page counter, (cluster << 16) | (rank << 8) | warp.
 enum WaitTag : int {
@@ -391,14 +364,13 @@ __device__ __forceinline__ int32_t read_page_id(const Params& p, int b, int pg) 
 // of kNSt slots, each filled by kParts copies with their own barriers.
 template <bool kF8, bool kRoleS>
 __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const CUtensorMap* tm_kv,
-                             const CUtensorMap* tm_pe, int cid, uint32_t partner, bool prefetch_pages) {
+                             const CUtensorMap* tm_pe, int cid, uint32_t partner) {
   using C = Cfg<kF8>;
   constexpr int kNSt = kRoleS ? C::kNStS : C::kNStO;
   constexpr int kSlot = kRoleS ? C::kSlotS : C::kSlotO;
   constexpr int kParts = kRoleS ? C::kPartsS : C::kPartsO;
   constexpr int kBoxes = kRoleS ? C::kBoxesPartS : C::kBoxesPartO;
   constexpr uint32_t kPartBytes = static_cast<uint32_t>(kBoxes * C::kBox);
-  constexpr uint32_t kPageBytes = kPage * (kDL + kDR) * C::kEsz;
   static_assert(kNSt * kParts <= 9, "ring parts");
   volatile int* abort = &ctrl->abort;
   UnitIter it;
@@ -410,11 +382,6 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
   // phase (i / kNQ) & 1
   constexpr uint32_t kNQ = kNSt * kParts;
   uint32_t copies = 0;
-  // With prefetch_pages, pages are pulled into L2 kPrefetchAhead pages
-  // before this producer copies them.
-  PageCursor ahead;
-  ahead.init(p, cid);
-  uint32_t pf = 0;
   // the queries of the unit after the current one are pulled into L2 too
   // (the softmax loads them into TMEM at the unit boundary)
   UnitIter nxt;
@@ -440,14 +407,6 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
       }
     }
     for (int pg = u.p0; pg < u.p1 && ok; ++pg, ++j) {
-      if (prefetch_pages) {
-        int pb, ppg;
-        while (pf < j + kPrefetchAhead && ahead.next(pb, ppg)) {
-          const int32_t pid = __ldg(p.page_table + static_cast<int64_t>(pb) * p.pt_stride + ppg);
-          if (pid >= 0 && pid < p.num_pages) prefetch_l2_bulk(p.kv + static_cast<int64_t>(pid) * kPageBytes, kPageBytes);
-          ++pf;
-        }
-      }
       const int st = j % kNSt;
       const uint32_t ph = (j / kNSt) & 1;
       const int32_t pid = read_page_id(p, u.b, pg);
@@ -747,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =========================== S CTA ===========================
     uint8_t* ring = data;
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, cid, partner, rank == 0);
+      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, cid, partner);
     } else if (warp == 1) {
       // QK issuer: the whole warp runs the loop and one elected lane issues
       // (a converged warp keeps the tensor pipe full with N = 64 MMAs), so
@@ -1023,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows_real = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
     const PSlots ps(kF8, rows_real);
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, cid, partner, false);
+      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, cid, partner);
     } else if (warp == 3) {
       // ---- waiter: gets page j ready for PV (c_kv landed, tail rows zeroed,
       // P arrived, O free and rescaled) while the MMA warp issues PV(j - 1);
