@@ -132,7 +132,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // tm_o: the O CTA's c_kv boxes, tm_pe: the e4m3 k_pe part (64-byte rows,
 // 64-byte swizzle, 2-D).
 struct Maps {
-  CUtensorMap s, o, pe;
+  CUtensorMap s, o, pe, qn, qp;
 };
 
 int make_maps(const void* kv, int num_pages, bool f8, Maps* m) {
@@ -168,6 +168,28 @@ int make_maps(const void* kv, int num_pages, bool f8, Maps* m) {
   return MLA_OK;
 }
 
+// Query rows as copied into the S CTA's ring (64 rows per copy, laid out
+// like a page): q_nope as 8 boxes of 64 values, q_pe as one.
+int make_qmaps(const void* q_nope, const void* q_pe, int64_t rows, Maps* m) {
+  auto enc = encode_fn();
+  if (!enc) return MLA_ERR_CUDA;
+  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(rows), 8};
+  cuuint64_t gstr[2] = {1024, 128};
+  cuuint32_t box[3] = {64, 64, 8};
+  CUresult r = enc(&m->qn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_nope), gdim, gstr, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+  cuuint64_t gdim2[2] = {64, static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstr2[1] = {128};
+  cuuint32_t box2[2] = {64, 64};
+  r = enc(&m->qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_pe), gdim2, gstr2, box2, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
@@ -199,6 +221,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   if (workspace_bytes < lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   Maps maps;
   if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
+  if ((rc = make_qmaps(q_nope, q_pe, static_cast<int64_t>(d->batch) * R, &maps)) != MLA_OK) return rc;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Params p;
@@ -222,6 +245,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.num_pages = d->num_pages;
   p.max_pages = d->max_pages_per_req;
   p.pt_stride = d->page_table_stride;
+  p.unit_cost = mla::unit_cost_pages(f8, R < mla::kRows ? R : mla::kRows);
   p.scale = scale;
   p.kv_scale = f8 ? kv_scale : 1.f;
   p.timeout_ns = kTimeoutNs;
@@ -248,8 +272,10 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe)
-                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe);
+  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe, maps.qn,
+                                          maps.qp)
+                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe,
+                                          maps.qn, maps.qp);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
@@ -451,6 +477,7 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   if ((rc = noalloc_scratch(dev, &ws)) != MLA_OK) return rc;
   Maps maps;
   if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
+  if ((rc = make_qmaps(q_nope, q_pe, static_cast<int64_t>(d->batch) * R, &maps)) != MLA_OK) return rc;
 
   Params p;
   p.q_nope = static_cast<const uint8_t*>(q_nope);
@@ -473,6 +500,7 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   p.num_pages = d->num_pages;
   p.max_pages = d->max_pages_per_req;
   p.pt_stride = d->page_table_stride;
+  p.unit_cost = mla::unit_cost_pages(f8, R < mla::kRows ? R : mla::kRows);
   p.scale = scale;
   p.kv_scale = f8 ? kv_scale : 1.f;
   p.timeout_ns = kTimeoutNs;
@@ -495,8 +523,10 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe)
-                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe);
+  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe, maps.qn,
+                                          maps.qp)
+                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe,
+                                          maps.qn, maps.qp);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;

@@ -56,8 +56,9 @@ constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..2
 constexpr int kCtrlBytes = 512;
 // Schedule weight of starting a request piece, in pages: a cluster pays a
 // fixed cost per piece it starts (queries into TMEM, pipeline refill,
-// epilogue), measured on GB300 at about the time of 8 to 12 pages.
-constexpr int kUnitCostPages = 10;
+// epilogue).  Measured on GB300: about 6 pages' time for row blocks of at
+// most 64 rows (bf16), about 10 for larger blocks and for e4m3.
+__host__ __device__ constexpr int unit_cost_pages(bool f8, int rows) { return (!f8 && rows <= 64) ? 6 : 10; }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy output rescale: O is rescaled only when a row's running max grows by
@@ -83,13 +84,9 @@ struct Cfg {
   static constexpr int kSlotO = kNBoxLat * kBox;
   static constexpr int kNStS = kF8 ? 6 : 3;
   static constexpr int kNStO = kF8 ? 6 : 3;
-  // A ring slot may be filled by several copies ("parts", each with its own
-  // full/empty barrier) so that MMAs start before the whole page landed.
-  // Measured on GB300: three 24 KB copies per page instead of one 72 KB
-  // copy raise the copy latency about threefold, so a page is one copy.
-  static constexpr int kPartsS = 1;
+  // One copy per page (measured on GB300: three 24 KB copies per page
+  // instead of one 72 KB copy raise the copy latency about threefold).
   static constexpr int kBoxesPartS = kF8 ? 4 : 9;   // boxes of the c_kv / whole-row map per copy
-  static constexpr int kPartsO = 1;
   static constexpr int kBoxesPartO = kF8 ? 4 : 8;
   static constexpr int kPBytes = kRows * kPage * kEsz;  // one P tile
   static constexpr int kPRow = kPage * kEsz;            // bytes of one P row (128 or 64)
@@ -157,8 +154,8 @@ struct PSlots {
 constexpr int kMaxPSlots = 4;
 
 struct __align__(8) Ctrl {
-  uint64_t kv_full[9];   // one per ring part: slot * parts + part
-  uint64_t kv_empty[9];
+  uint64_t kv_full[6];   // one per ring slot
+  uint64_t kv_empty[6];
   uint64_t s_full[kNS];
   uint64_t s_empty[kNS];
   uint64_t q_full;  // queries of the unit loaded into TMEM
@@ -192,6 +189,7 @@ struct Params {
   int32_t* cinfo;          // [C][3] = slice start, slice end, first request
   int32_t B, H, Q, R, G, C;
   int32_t num_pages, max_pages, pt_stride;
+  int32_t unit_cost;       // schedule weight of a request piece, in pages
   float scale, kv_scale;
   uint64_t timeout_ns;
 };
@@ -260,19 +258,19 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   if (tid == 0) p.prefix[0] = 0;
   __syncthreads();
   // Cluster slices are cut in a weighted order: request b occupies
-  // kUnitCostPages start-up units and then its pages, so clusters whose
+  // p.unit_cost start-up units and then its pages, so clusters whose
   // slice starts many pieces get fewer pages.  A weighted position maps to
   // the page at that point (start-up units map to the request's first page).
   const int64_t T = p.prefix[p.B];
-  const int64_t W = T + static_cast<int64_t>(kUnitCostPages) * p.B;
+  const int64_t W = T + static_cast<int64_t>(p.unit_cost) * p.B;
   auto page_at = [&](int64_t x) -> int {
-    int lo = 0, hi = p.B - 1;  // last request b with prefix[b] + kUnitCostPages * b <= x
+    int lo = 0, hi = p.B - 1;  // last request b with prefix[b] + unit_cost * b <= x
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.prefix[mid] + static_cast<int64_t>(kUnitCostPages) * mid <= x) lo = mid; else hi = mid - 1;
+      if (p.prefix[mid] + static_cast<int64_t>(p.unit_cost) * mid <= x) lo = mid; else hi = mid - 1;
     }
     const int64_t np = p.prefix[lo + 1] - p.prefix[lo];
-    int64_t off = x - p.prefix[lo] - static_cast<int64_t>(kUnitCostPages) * lo - kUnitCostPages;
+    int64_t off = x - p.prefix[lo] - static_cast<int64_t>(p.unit_cost) * lo - p.unit_cost;
     off = off < 0 ? 0 : (off > np ? np : off);
     return static_cast<int>(p.prefix[lo] + off);
   };
@@ -337,7 +335,7 @@ struct UnitIter {
 enum WaitTag : int {
   kWaitProdEmptyS = 1, kWaitProdEmptyO, kWaitQFull, kWaitKvFullS, kWaitSEmpty, kWaitSFull, kWaitPEmptyS,
   kWaitMlEmpty, kWaitKvFullO, kWaitPFullO, kWaitOEmpty, kWaitRescDone, kWaitPFullCorr, kWaitPvPrev,
-  kWaitOFull, kWaitMlFull, kWaitHandoff, kWaitSPrevUnit, kWaitPvReady, kWaitPvTaken
+  kWaitOFull, kWaitMlFull, kWaitHandoff, kWaitSPrevUnit, kWaitPvReady, kWaitPvTaken, kWaitQEntry
 };
 
 __device__ __forceinline__ void raise_timeout(const Params& p, Ctrl* ctrl, uint32_t partner_rank, int tag,
@@ -360,82 +358,96 @@ __device__ __forceinline__ int32_t read_page_id(const Params& p, int b, int pg) 
   return pid;
 }
 
+// Ring entries of the bf16 S CTA holding a unit's query rows: 64 rows per
+// entry, laid out like a page (8 boxes of q_nope, the 9th of q_pe).
+__device__ __forceinline__ int q_entries(int rows_real) { return (rows_real + 63) / 64; }
+
 // TMA producer shared by both roles: streams the slice's pages into a ring
-// of kNSt slots, each filled by kParts copies with their own barriers.
+// of kNSt slots (entry i: slot i % kNSt, phase (i / kNSt) & 1).  The bf16 S
+// CTA streams, ahead of each unit's pages, the unit's query rows as well
+// (q_entries entries), which the softmax warps move into TMEM: coalesced
+// copies issued as soon as a slot frees, instead of per-row loads at the
+// unit boundary.
 template <bool kF8, bool kRoleS>
 __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const CUtensorMap* tm_kv,
-                             const CUtensorMap* tm_pe, int cid, uint32_t partner) {
+                             const CUtensorMap* tm_pe, const CUtensorMap* tm_qn, const CUtensorMap* tm_qp, int cid,
+                             uint32_t partner) {
   using C = Cfg<kF8>;
   constexpr int kNSt = kRoleS ? C::kNStS : C::kNStO;
   constexpr int kSlot = kRoleS ? C::kSlotS : C::kSlotO;
-  constexpr int kParts = kRoleS ? C::kPartsS : C::kPartsO;
-  constexpr int kBoxes = kRoleS ? C::kBoxesPartS : C::kBoxesPartO;
-  constexpr uint32_t kPartBytes = static_cast<uint32_t>(kBoxes * C::kBox);
-  static_assert(kNSt * kParts <= 9, "ring parts");
+  constexpr uint32_t kCopyBytes = static_cast<uint32_t>((kRoleS ? C::kBoxesPartS : C::kBoxesPartO) * C::kBox);
   volatile int* abort = &ctrl->abort;
+  const int g = static_cast<int>(cluster_ctarank() >> 1);
+  const int rows_real = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
+  const int qe = (kRoleS && !kF8) ? q_entries(rows_real) : 0;
   UnitIter it;
   it.init(p, cid);
   Unit u;
-  uint32_t j = 0;
+  uint32_t j = 0;  // pages
+  uint32_t i = 0;  // ring entries
   bool ok = true;
-  // copy i (page i / kParts, part i % kParts) uses ring part i % kNQ with
-  // phase (i / kNQ) & 1
-  constexpr uint32_t kNQ = kNSt * kParts;
-  uint32_t copies = 0;
-  // the queries of the unit after the current one are pulled into L2 too
-  // (the softmax loads them into TMEM at the unit boundary)
+  // waits for the slot of entry i; returns its full barrier and address
+  auto acquire = [&](uint32_t& bar, uint8_t*& slot) -> bool {
+    const int st = static_cast<int>(i % kNSt);
+    if (!mbar_wait(smem_u32(&ctrl->kv_empty[st]), ((i / kNSt) & 1) ^ 1, abort, p.timeout_ns)) {
+      raise_timeout(p, ctrl, partner, kRoleS ? kWaitProdEmptyS : kWaitProdEmptyO, j);
+      return false;
+    }
+    bar = smem_u32(&ctrl->kv_full[st]);
+    slot = ring + st * kSlot;
+    return true;
+  };
+  // the next unit's query rows are pulled into L2 as well
   UnitIter nxt;
   nxt.init(p, cid);
   Unit un_next;
   bool have_next = kRoleS && nxt.next(un_next);
-  if (have_next) {  // the first unit's queries, which the softmax loads right away
-    const int g = static_cast<int>(cluster_ctarank() >> 1);
-    const int rows = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
-    const int64_t row0 = static_cast<int64_t>(un_next.b) * p.Q * p.H + g * kRows;
-    prefetch_l2_bulk(p.q_nope + row0 * kDL * 2, static_cast<uint32_t>(rows) * kDL * 2);
-    prefetch_l2_bulk(p.q_pe + row0 * kDR * 2, static_cast<uint32_t>(rows) * kDR * 2);
-  }
+  auto prefetch_q = [&](const Unit& w) {
+    const int64_t row0 = static_cast<int64_t>(w.b) * p.Q * p.H + g * kRows;
+    prefetch_l2_bulk(p.q_nope + row0 * kDL * 2, static_cast<uint32_t>(rows_real) * kDL * 2);
+    prefetch_l2_bulk(p.q_pe + row0 * kDR * 2, static_cast<uint32_t>(rows_real) * kDR * 2);
+  };
+  if (have_next) prefetch_q(un_next);
   while (ok && it.next(u)) {
-    if (kRoleS) {  // every S CTA: its own row block's query rows
+    if (kRoleS) {
       have_next = have_next && nxt.next(un_next);
-      if (have_next) {
-        const int g = static_cast<int>(cluster_ctarank() >> 1);
-        const int rows = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
-        const int64_t row0 = static_cast<int64_t>(un_next.b) * p.Q * p.H + g * kRows;
-        prefetch_l2_bulk(p.q_nope + row0 * kDL * 2, static_cast<uint32_t>(rows) * kDL * 2);
-        prefetch_l2_bulk(p.q_pe + row0 * kDR * 2, static_cast<uint32_t>(rows) * kDR * 2);
+      if (have_next) prefetch_q(un_next);
+    }
+    for (int e = 0; e < qe && ok; ++e) {
+      uint32_t bar;
+      uint8_t* slot;
+      if (!acquire(bar, slot)) {
+        ok = false;
+        break;
       }
+      const int row = static_cast<int>(static_cast<int64_t>(u.b) * p.Q * p.H + g * kRows + 64 * e);
+      mbar_expect_tx(bar, static_cast<uint32_t>(C::kSlotS));
+      tma_load_3d(smem_u32(slot), tm_qn, 0, row, 0, bar);
+      tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_qp, 0, row, bar);
+      ++i;
     }
     for (int pg = u.p0; pg < u.p1 && ok; ++pg, ++j) {
-      const int st = j % kNSt;
-      const uint32_t ph = (j / kNSt) & 1;
       const int32_t pid = read_page_id(p, u.b, pg);
       const int y = pid * kPage;
-      uint8_t* slot = ring + st * kSlot;
-#pragma unroll
-      for (int part = 0; part < kParts; ++part) {
-        const int q = st * kParts + part;
-        if (!mbar_wait(smem_u32(&ctrl->kv_empty[q]), ph ^ 1, abort, p.timeout_ns)) {
-          raise_timeout(p, ctrl, partner, kRoleS ? kWaitProdEmptyS : kWaitProdEmptyO, j);
-          ok = false;
-          break;
-        }
-        const uint32_t bar = smem_u32(&ctrl->kv_full[q]);
-        const bool pe = kRoleS && kF8;  // e4m3 S CTA: the k_pe box comes by its own map
-        mbar_expect_tx(bar, kPartBytes + (pe ? static_cast<uint32_t>(C::kPeBytes) : 0u));
-        // 3-D boxes: kBoxes 128-byte columns x 64 token rows, box-major and
-        // 128-byte swizzled
-        tma_load_3d(smem_u32(slot + part * kPartBytes), tm_kv, 0, y, part * kBoxes, bar);
-        if (pe) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_pe, kDL, y, bar);
-        ++copies;
+      uint32_t bar;
+      uint8_t* slot;
+      if (!acquire(bar, slot)) {
+        ok = false;
+        break;
       }
+      const bool pe = kRoleS && kF8;  // e4m3 S CTA: the k_pe box comes by its own map
+      mbar_expect_tx(bar, kCopyBytes + (pe ? static_cast<uint32_t>(C::kPeBytes) : 0u));
+      // one 3-D box: 128-byte columns x 64 token rows, box-major, 128-byte swizzled
+      tma_load_3d(smem_u32(slot), tm_kv, 0, y, 0, bar);
+      if (pe) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_pe, kDL, y, bar);
+      ++i;
       MLA_TRACE_POINT(kRoleS ? 0 : 1, 0, j);
     }
   }
-  // Drain: every copy issued into each part must have landed before exit.
-  for (uint32_t q = 0; q < kNQ && q < copies; ++q) {
-    const uint32_t last = copies - 1 - ((copies - 1 - q) % kNQ);  // last copy into part q
-    const uint32_t ph = (last / kNQ) & 1;
+  // Drain: every copy issued into each slot must have landed before exit.
+  for (uint32_t q = 0; q < static_cast<uint32_t>(kNSt) && q < i; ++q) {
+    const uint32_t last = i - 1 - ((i - 1 - q) % kNSt);  // last entry in slot q
+    const uint32_t ph = (last / kNSt) & 1;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(smem_u32(&ctrl->kv_full[q]), ph) && globaltimer_ns() - t0 < p.timeout_ns) {
     }
@@ -610,6 +622,32 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
   }
 }
 
+// bf16 query row from a ring entry into TMEM lane r: 16-byte chunks
+// [c0, c0 + 36) (chunk c = box c / 8 (8 of q_nope, then q_pe), piece c % 8 of
+// the 128-byte-swizzled row rq).  src = the row's first box row, or null
+// for a padding row (zeros).
+__device__ __forceinline__ void load_q_row_smem(const uint8_t* src, int rq, uint32_t taddr_row, int c0) {
+#pragma unroll
+  for (int c = 0; c < 36; c += 12) {
+    uint4 v[12];
+#pragma unroll
+    for (int k = 0; k < 12; ++k) {
+      const int cc = c0 + c + k;
+      v[k] = src ? *reinterpret_cast<const uint4*>(src + (cc >> 3) * 8192 + (((cc & 7) ^ (rq & 7)) << 4))
+                 : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int s4 = 0; s4 < 3; ++s4) {
+      const uint32_t w[16] = {v[4 * s4].x,     v[4 * s4].y,     v[4 * s4].z,     v[4 * s4].w,
+                              v[4 * s4 + 1].x, v[4 * s4 + 1].y, v[4 * s4 + 1].z, v[4 * s4 + 1].w,
+                              v[4 * s4 + 2].x, v[4 * s4 + 2].y, v[4 * s4 + 2].z, v[4 * s4 + 2].w,
+                              v[4 * s4 + 3].x, v[4 * s4 + 3].y, v[4 * s4 + 3].z, v[4 * s4 + 3].w};
+      tmem_st16(taddr_row + (c0 + c + 4 * s4) * 4, w);
+    }
+  }
+  tmem_wait_st();
+}
+
 // e4m3 queries: the per-row scale load_q_row uses (amax / 448), computed by
 // the softmax group that does not load the queries itself.
 __device__ __forceinline__ float query_scale(const Params& p, int b, int g, int r) {
@@ -643,7 +681,8 @@ __device__ __forceinline__ float query_scale(const Params& p, int b, int g, int 
 template <bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_s,
-                      const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_pe) {
+                      const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_pe,
+                      const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp) {
   using C = Cfg<kF8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* data = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -657,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 9; ++i) {
+    for (int i = 0; i < 6; ++i) {
       mbar_init(smem_u32(&ctrl->kv_full[i]), 1);
       mbar_init(smem_u32(&ctrl->kv_empty[i]), 1);
     }
@@ -706,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =========================== S CTA ===========================
     uint8_t* ring = data;
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, cid, partner);
+      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, &tm_qn, &tm_qp, cid, partner);
     } else if (warp == 1) {
       // QK issuer: the whole warp runs the loop and one elected lane issues
       // (a converged warp keeps the tensor pipe full with N = 64 MMAs), so
@@ -717,17 +756,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0, un = 0;
       bool ok = true;
       int why = 0;
+      const int qe = kF8 ? 0 : q_entries(p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
       while (ok && it.next(u)) {
         if (!mbar_wait_warp(smem_u32(&ctrl->q_full), un & 1, abort, p.timeout_ns)) {
           ok = false;
           why = kWaitQFull;
           break;
         }
+        // the unit's query entries were moved into TMEM: their slots go back
+        // to the producer (entries j + qe * un ..)
+        for (int e = 0; e < qe; ++e)
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->kv_empty[(j + qe * un + e) % C::kNStS]));
         ++un;
         for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
-          const int st = j % C::kNStS;
+          const uint32_t ri = j + qe * un;  // ring entry of this page
+          const int st = ri % C::kNStS;
           const int sb = j % kNS;
-          const uint32_t kph = (j / C::kNStS) & 1;
+          const uint32_t kph = (ri / C::kNStS) & 1;
           if (lane == 0) MLA_TRACE_POINT(0, 9, j);
           if (!mbar_wait_warp(smem_u32(&ctrl->s_empty[sb]), ((j / kNS) & 1) ^ 1, abort, p.timeout_ns)) {
             ok = false;
@@ -801,6 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool real = rr < p.R;  // rows past H * q_len are padding: nothing of theirs is sent
       const PSlots ps(kF8, p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
       const int qi = real ? rr / p.H : p.Q - 1;
+      const int qe = kF8 ? 0 : q_entries(p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
       UnitIter it;
       it.init(p, cid);
       Unit u;
@@ -827,7 +873,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kF8) {
             qs = load_q_row<true>(p, u.b, g, r, tmem + lane_base);
           } else {
-            load_q_row<false, 36>(p, u.b, g, r, tmem + lane_base, 36 * gg);
+            // the producer copied this unit's query rows into ring entries
+            // j + qe * un ..; half gg moves chunks [36 gg, 36 gg + 36) of row r
+            const uint32_t iq = j + qe * un;
+            bool got = true;
+            for (int e = 0; e < qe && got; ++e)
+              got = mbar_wait_warp<false, true>(smem_u32(&ctrl->kv_full[(iq + e) % C::kNStS]),
+                                                ((iq + e) / C::kNStS) & 1, abort, p.timeout_ns);
+            if (!got) {
+              ok = false;
+              why = kWaitQEntry;
+              break;
+            }
+            const int e = r >> 6, rq = r & 63;
+            const uint8_t* src = (real && e < qe) ? ring + ((iq + e) % C::kNStS) * C::kSlotS + rq * 128 : nullptr;
+            load_q_row_smem(src, rq, tmem + lane_base, 36 * gg);
           }
           tc_fence_before();
           __syncwarp();
@@ -982,12 +1042,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows_real = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
     const PSlots ps(kF8, rows_real);
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, cid, partner);
+      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, &tm_qn, &tm_qp, cid, partner);
     } else if (warp == 3) {
       // ---- waiter: gets page j ready for PV (c_kv landed, tail rows zeroed,
       // P arrived, O free and rescaled) while the MMA warp issues PV(j - 1);
       // the MMA warp then waits on one barrier per page
-      static_assert(C::kPartsO == 1, "the O ring holds whole pages");
       UnitIter it;
       it.init(p, cid);
       Unit u;
@@ -1314,9 +1373,7 @@ __global__ void __launch_bounds__(128) mla_gather_kernel(const __grid_constant__
   if (threadIdx.x == 0) {
     // exactly the loads of the decode kernel's S CTA
     mbar_expect_tx(smem_u32(bar), C::kSlotS);
-    for (int part = 0; part < C::kPartsS; ++part)
-      tma_load_3d(smem_u32(page + part * C::kBoxesPartS * C::kBox), &tm_s, 0, pid * kPage, part * C::kBoxesPartS,
-                  smem_u32(bar));
+    tma_load_3d(smem_u32(page), &tm_s, 0, pid * kPage, 0, smem_u32(bar));
     if constexpr (kF8) tma_load_2d(smem_u32(page + C::kNBoxLat * C::kBox), &tm_pe, kDL, pid * kPage, smem_u32(bar));
   }
   if (!mbar_wait(smem_u32(bar), 0, abort_flag, gp.timeout_ns)) {
