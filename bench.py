@@ -59,6 +59,27 @@ def algorithmic_work(wl):
     return nbytes, flops, unique_rows
 
 
+def profiled_traffic(config: str):
+    """DRAM bytes (read + write) of one attention-kernel launch on this batch,
+    from the ncu capture summarised in profiles/, or None when the kernel
+    sources changed since that capture (or the batch was not captured)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        h.update(open(fp, "rb").read())
+    if h.hexdigest() != rec["sha256"]:
+        return None
+    return rec["dram_bytes_per_launch"].get(config)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -346,7 +367,7 @@ def run_ours(args):
     else:
         achieved, peak, unit_r = flops / (k1 * 1e-3) / 1e12, flop_peak, "TFLOP/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit_r, "frac": achieved / peak,
-                "traffic": None,
+                "traffic": profiled_traffic(args.config), "traffic_unit": "bytes per launch (ncu dram read + write)",
                 "peak_source": peak_src + (" (e4m3 = 2x bf16, nominal ratio)" if f8 and bound == "tensor" else ""),
                 "kernel": "mla_decode_kernel", "alg_bytes": nbytes, "alg_flops": flops,
                 "step_frac": max(t_bytes, t_flops) / (ms * 1e-3)}
