@@ -401,7 +401,8 @@ def run_ours(args):
             "kernel_ms": {"schedule": float(np.mean(k0_ms)), "attention": k1, "combine": float(np.mean(k2_ms))},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            # schedule, (e4m3: query scales,) attention, combine
+            "gpu_launches": (4 if f8 else 3) * args.steps,
             "clocks": clocks,
             "device_status": status,
             "parity_sample": parity,

@@ -22,7 +22,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // partial outputs | partial log-sum-exps].  Sized by B, the cluster count
 // and the number of row blocks only.
 struct Layout {
-  size_t status, prefix, cinfo, o_part, lse_part, total;
+  size_t status, prefix, cinfo, o_part, lse_part, qscale, total;
 };
 
 Layout workspace_layout(int B, int C, int G) {
@@ -32,7 +32,8 @@ Layout workspace_layout(int B, int C, int G) {
   l.cinfo = l.prefix + align256(static_cast<size_t>(B + 1) * 4);
   l.o_part = l.cinfo + align256(static_cast<size_t>(C) * 3 * 4);
   l.lse_part = l.o_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * mla::kDL * 4);
-  l.total = l.lse_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * 4);
+  l.qscale = l.lse_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * 4);
+  l.total = l.qscale + align256(static_cast<size_t>(B) * G * mla::kRows * 4);  // e4m3 query scales
   return l;
 }
 
@@ -236,6 +237,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.status = reinterpret_cast<int32_t*>(ws + lay.status);
   p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
   p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
+  p.qscale = reinterpret_cast<float*>(ws + lay.qscale);
   p.B = d->batch;
   p.H = d->num_heads;
   p.Q = d->q_len;
@@ -258,6 +260,10 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   if (!mark(0)) return MLA_ERR_CUDA;
   mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  if (f8) {  // per-row e4m3 query scales
+    mla::mla_qscale_kernel<<<static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  }
   if (!mark(1)) return MLA_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
@@ -491,6 +497,7 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   p.status = reinterpret_cast<int32_t*>(ws + lay.status);
   p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
   p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
+  p.qscale = reinterpret_cast<float*>(ws + lay.qscale);
   p.B = d->batch;
   p.H = d->num_heads;
   p.Q = d->q_len;
@@ -511,6 +518,10 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   if (cudaMemsetAsync(p.status, 0, 16, stream) != cudaSuccess) return MLA_ERR_CUDA;
   mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  if (f8) {
+    mla::mla_qscale_kernel<<<static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * G * C, 1, 1);
   cfg.blockDim = dim3(mla::kThreads, 1, 1);

@@ -187,6 +187,7 @@ struct Params {
   int32_t* status;         // [4]: status bits, timeout diagnostics
   int32_t* prefix;         // [B+1] page prefix sums
   int32_t* cinfo;          // [C][3] = slice start, slice end, first request
+  float* qscale;           // [B * R] e4m3 query scales (e4m3 cache only)
   int32_t B, H, Q, R, G, C;
   int32_t num_pages, max_pages, pt_stride;
   int32_t unit_cost;       // schedule weight of a request piece, in pages
@@ -203,7 +204,7 @@ __device__ uint64_t g_mla_cluster_times[1024][4];
 __device__ int g_mla_trace_cid;  // the cluster whose events are stamped
 #define MLA_TRACE_POINT(role, ev, j)                                                                     \
   do {                                                                                                   \
-    if (cluster_id_x() == static_cast<uint32_t>(g_mla_trace_cid) && (j) < 1024)                         \
+    if (cluster_id_x() == static_cast<uint32_t>(g_mla_trace_cid) && cluster_ctarank() < 2 && (j) < 1024) \
       g_mla_trace[(role)][(ev)][(j)] = globaltimer_ns();                                                 \
   } while (0)
 #else
@@ -286,6 +287,30 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     p.cinfo[3 * c + 1] = e;
     p.cinfo[3 * c + 2] = lo;
   }
+}
+
+// ---------------------------------------------------------------- K0b
+// e4m3 cache: per query row r of request b, the scale of its e4m3 split,
+// max |q| / 448 over the 576 values (1 for an all-zero row).  One warp per row.
+__global__ void __launch_bounds__(256) mla_qscale_kernel(Params p) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<int64_t>(p.B) * p.R) return;
+  const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
+  const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + row * kDR * 2);
+  float amax = 0.f;
+  for (int c = lane; c < 72; c += 32) {
+    const uint4 v = c < 64 ? __ldg(qn + c) : __ldg(qp + (c - 64));
+    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) p.qscale[row] = amax > 0.f ? amax / 448.f : 1.f;
 }
 
 // One request's piece inside a cluster's slice.
@@ -520,13 +545,13 @@ __device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g,
   }
 }
 
-// Loads query row r of row block g for request b into TMEM lane r (packed
-// along K: 2 bf16 or 4 e4m3 per column).  bf16: only the 16-byte chunks
-// [c0, c0 + kN) of the row (chunk c = 8 values: c < 64 from q_nope, else
-// q_pe), 12 loads in flight per round.  e4m3 (whole row, kN ignored): returns
-// the row's quantisation scale (value = code * scale).
+// Loads the 16-byte chunks [c0, c0 + kN) of query row r of row block g for
+// request b (chunk c = 8 values: c < 64 from q_nope, else q_pe) into TMEM
+// lane r, packed along K: 2 bf16 or 4 e4m3 per column.  e4m3: both terms
+// of the split with the row's scale qs_in, which is returned.
 template <bool kF8, int kN = 72>
-__device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r, uint32_t taddr_row, int c0 = 0) {
+__device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r, uint32_t taddr_row, int c0 = 0,
+                                            float qs_in = 1.f) {
   const int rr = g * kRows + r;
   const bool real = rr < p.R;
   const uint4* qn = nullptr;
@@ -567,21 +592,9 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
     tmem_wait_st();
     return 1.f;
   } else {
-    float amax = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < 72; c += 12) {
-      uint32_t v[6][8];
-#pragma unroll
-      for (int k = 0; k < 6; ++k) pair(c + 2 * k, v[k]);
-#pragma unroll
-      for (int k = 0; k < 6; ++k)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[k][e]));
-          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
-    }
-    const float qs = amax > 0.f ? amax / 448.f : 1.f;
+    // e4m3: chunks [c0, c0 + kN) (kN a multiple of 8) as hi + lo terms with
+    // the row's scale qs_in (value = code * qs)
+    const float qs = qs_in;
     const float inv = 1.f / qs;
     // two e4m3 codes for a pair of scaled values: hi = e4m3(x), lo = e4m3(x - hi)
     auto split2 = [](float2 x, uint32_t& hi16, uint32_t& lo16) {
@@ -593,8 +606,9 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
       hi16 = h;
       lo16 = l;
     };
+    static_assert(kN % 8 == 0, "rounds of 8 chunks");
 #pragma unroll 1
-    for (int c = 0; c < 72; c += 8) {  // 64 values -> 16 columns of each term
+    for (int c = c0; c < c0 + kN; c += 8) {  // 64 values -> 16 columns of each term
       uint32_t v8[4][8];
 #pragma unroll
       for (int k = 0; k < 4; ++k) pair(c + 2 * k, v8[k]);
@@ -648,35 +662,6 @@ __device__ __forceinline__ void load_q_row_smem(const uint8_t* src, int rq, uint
   tmem_wait_st();
 }
 
-// e4m3 queries: the per-row scale load_q_row uses (amax / 448), computed by
-// the softmax group that does not load the queries itself.
-__device__ __forceinline__ float query_scale(const Params& p, int b, int g, int r) {
-  const int rr = g * kRows + r;
-  if (rr >= p.R) return 1.f;
-  const int i = rr / p.H, h = rr % p.H;
-  const int64_t row = (static_cast<int64_t>(b) * p.Q + i) * p.H + h;
-  const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
-  const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + row * kDR * 2);
-  float amax = 0.f;
-#pragma unroll 1
-  for (int c = 0; c < 72; c += 12) {
-    uint32_t v[6][8];
-#pragma unroll
-    for (int k = 0; k < 6; ++k) {
-      const int cc = c + 2 * k;
-      ldg_v8(cc < 64 ? static_cast<const void*>(qn + cc) : static_cast<const void*>(qp + (cc - 64)), v[k]);
-    }
-#pragma unroll
-    for (int k = 0; k < 6; ++k)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[k][e]));
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
-  }
-  return amax > 0.f ? amax / 448.f : 1.f;
-}
-
 // ---------------------------------------------------------------- K1
 template <bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -704,8 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->s_full[i]), 1);
       mbar_init(smem_u32(&ctrl->s_empty[i]), kRowWarps / 2);  // the group that read the page
     }
-    // the warps that load the queries: both groups (bf16) or group 0 (e4m3)
-    mbar_init(smem_u32(&ctrl->q_full), kF8 ? kRowWarps / 2 : kRowWarps);
+    mbar_init(smem_u32(&ctrl->q_full), kRowWarps);  // both groups load the queries
     for (int i = 0; i < kMaxPSlots; ++i) {
       mbar_init(smem_u32(&ctrl->p_full[i]), 1);  // one arm (expect_tx) by the O MMA warp + P bytes
       mbar_init(smem_u32(&ctrl->p_empty[i]), 1);
@@ -774,15 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sb = j % kNS;
           const uint32_t kph = (ri / C::kNStS) & 1;
           if (lane == 0) MLA_TRACE_POINT(0, 9, j);
-          if (!mbar_wait_warp(smem_u32(&ctrl->s_empty[sb]), ((j / kNS) & 1) ^ 1, abort, p.timeout_ns)) {
-            ok = false;
-            why = kWaitSEmpty;
-            break;
-          }
-          if (!mbar_wait_warp(smem_u32(&ctrl->kv_full[st]), kph, abort, p.timeout_ns)) {
-            ok = false;
-            why = kWaitKvFullS;
-            break;
+          {  // S buffer free and page landed, polled together
+            const uint32_t bars[4] = {smem_u32(&ctrl->s_empty[sb]), smem_u32(&ctrl->kv_full[st]), 0u, 0u};
+            const uint32_t pars[4] = {((j / kNS) & 1) ^ 1, kph, 0u, 0u};
+            if (!mbar_wait4_warp(bars, pars, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitKvFullS;
+              break;
+            }
           }
           if (lane == 0) MLA_TRACE_POINT(0, 1, j);
           tc_fence_after();
@@ -854,12 +837,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int why = 0;
       while (ok && it.next(u)) {
-        float qs = 1.f;
-        // bf16: both groups load half of every query row; e4m3: group 0 loads
-        // whole rows (the per-row scale needs all of it), group 1 computes
-        // the scale alone
+        // both groups load part of every query row (e4m3: with the row's scale
+        // from the pre-pass)
+        const float qs = (kF8 && real) ? p.qscale[static_cast<int64_t>(u.b) * p.R + rr] : 1.f;
         if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 11, un);
-        if (gg == 0 || !kF8) {
+        {
           // the queries of this unit replace the previous unit's in TMEM once
           // every QK of that unit is done: the S of its last page has landed
           // (one issuer: its commit covers all its earlier MMAs)
@@ -871,7 +853,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 12, un);
           if constexpr (kF8) {
-            qs = load_q_row<true>(p, u.b, g, r, tmem + lane_base);
+            if (gg == 0) load_q_row<true, 32>(p, u.b, g, r, tmem + lane_base, 0, qs);
+            else load_q_row<true, 40>(p, u.b, g, r, tmem + lane_base, 32, qs);
           } else {
             // the producer copied this unit's query rows into ring entries
             // j + qe * un ..; half gg moves chunks [36 gg, 36 gg + 36) of row r
@@ -894,8 +877,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // release the queries to the QK issuer
           if (lane == 0) mbar_arrive(smem_u32(&ctrl->q_full));
           if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 13, un);
-        } else if constexpr (kF8) {
-          qs = query_scale(p, u.b, g, r);
         }
         const float c2 = p.scale * kLog2e * (kF8 ? qs * p.kv_scale : 1.f);  // log2-domain score scale
         const int nvis = u.L - p.Q + qi + 1;
