@@ -114,21 +114,21 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = make_idesc(kF8, 128, 64, false, false);
   static constexpr uint32_t kIdescPV = make_idesc(kF8, 128, 256, false, true);
   static constexpr int kMlOff = kNStS * kSlotS;          // S CTA: (m0, l0, m1, l1)[128], one pair per group
-  static constexpr int kMrefOff = kMlOff + 4 * kRows * 4;  // S CTA: running max after a page [2 parities][128]
-  static constexpr int kDataS = kMrefOff + 2 * kRows * 4;
+  static constexpr int kPubOff = kMlOff + 4 * kRows * 4;  // S CTA: published row references [128] (unit tag, value)
+  static constexpr int kDataS = kPubOff + kRows * 8;
   // O CTA: P slots first (a slot's padding rows read on into what follows,
   // which must be shared memory of this CTA), then the c_kv ring, then the
-  // alphas that come with each P
+  // row references that come with each P
   static constexpr int kPOff = 0;
   static constexpr int kPRegion = kF8 ? 3 * 8192 : 4 * 8192;
   static constexpr int kRingOffO = kPOff + kPRegion;
-  static constexpr int kAlphaOff = kRingOffO + kNStO * kSlotO;
-  static constexpr int kAlphaBytes = kF8 ? 3 * kRows * 4 : 2 * kRows * 4;
-  static constexpr int kDataO = kAlphaOff + kAlphaBytes;
+  static constexpr int kRefOff = kRingOffO + kNStO * kSlotO;
+  static constexpr int kRefBytes = kF8 ? 3 * kRows * 4 : 2 * kRows * 4;
+  static constexpr int kDataO = kRefOff + kRefBytes;
   static constexpr int kData = kDataS > kDataO ? kDataS : kDataO;
   // dynamic smem = alignment slack + 1024-aligned data + control block
   static constexpr int kSmem = 1024 + kData + kCtrlBytes;
-  // bytes the S CTA sends per page and real query row: P row + its alpha
+  // bytes the S CTA sends per page and real query row: P row + its reference
   static constexpr uint32_t kPTxRow = kPRow + 4;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -140,7 +140,7 @@ struct Cfg {
 struct PSlots {
   int n;            // slots
   uint32_t stride;  // bytes from one slot to the next
-  int arows;        // alpha entries per slot
+  int arows;        // reference entries per slot
   __device__ PSlots(bool f8, int rows_real) {
     if (f8) {
       n = 3; stride = 8192; arows = kRows;
@@ -166,7 +166,6 @@ struct __align__(8) Ctrl {
   uint64_t resc_done[kMaxPSlots];
   uint64_t ml_full;
   uint64_t ml_empty;
-  uint64_t hb[2];  // S CTA: running max after page j published, per page parity (one group each)
   uint64_t pv_ready;  // O CTA: page j is ready for PV (waiter warp -> MMA warp)
   uint64_t pv_taken;  // O CTA: the MMA warp took page j (keeps the waiter one page ahead at most)
   uint64_t drain;
@@ -360,7 +359,7 @@ struct UnitIter {
 enum WaitTag : int {
   kWaitProdEmptyS = 1, kWaitProdEmptyO, kWaitQFull, kWaitKvFullS, kWaitSEmpty, kWaitSFull, kWaitPEmptyS,
   kWaitMlEmpty, kWaitKvFullO, kWaitPFullO, kWaitOEmpty, kWaitRescDone, kWaitPFullCorr, kWaitPvPrev,
-  kWaitOFull, kWaitMlFull, kWaitHandoff, kWaitSPrevUnit, kWaitPvReady, kWaitPvTaken, kWaitQEntry
+  kWaitOFull, kWaitMlFull, kWaitSPrevUnit, kWaitPvReady, kWaitPvTaken, kWaitQEntry
 };
 
 __device__ __forceinline__ void raise_timeout(const Params& p, Ctrl* ctrl, uint32_t partner_rank, int tag,
@@ -701,8 +700,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&ctrl->ml_empty), kRowWarps);
     mbar_init(smem_u32(&ctrl->pv_ready), 1);
     mbar_init(smem_u32(&ctrl->pv_taken), 1);
-    mbar_init(smem_u32(&ctrl->hb[0]), kRowWarps / 2);
-    mbar_init(smem_u32(&ctrl->hb[1]), kRowWarps / 2);
     mbar_init(smem_u32(&ctrl->drain), 1);
     ctrl->abort = 0;
     fence_barrier_init();
@@ -715,6 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&ctrl->tmem_base), 512);
     tmem_relinquish();
   }
+  if (role_s && threadIdx.x >= 128 && threadIdx.x < 256)  // published references: no unit yet
+    reinterpret_cast<uint64_t*>(data + C::kPubOff)[threadIdx.x - 128] = 0ull;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -814,17 +813,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp >= 4) {
       // ---- softmax: group gg (warps 4-7: 0, warps 8-11: 1) takes the pages
-      // j with j % 2 == gg; its thread r owns query row r.  The running max
-      // (the reference of P and of O) is handed from page j to page j + 1
-      // through mref_buf and hb; each group keeps its own partial sum, in
-      // the frame of the running max after its latest page.
+      // j with j % 2 == gg; its thread r owns query row r.  P of a page is
+      // computed against a reference (a running max of the row) that is
+      // sent with it; the O CTA brings every page to one frame.  Handlers
+      // share references through a published value per row (tagged with the
+      // unit), so pages rarely disagree; nothing waits for another page.
+      // Each group keeps its partial sum in the frame of its latest reference.
       const int r = (warp & 3) * 32 + lane;
       const int gg = (warp - 4) >> 2;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t p_remote = mapa(smem_u32(data + C::kPOff), partner);
-      const uint32_t alpha_remote = mapa(smem_u32(data + C::kAlphaOff), partner);
+      const uint32_t ref_remote = mapa(smem_u32(data + C::kRefOff), partner);
       const uint32_t mlfull_remote = mapa(smem_u32(&ctrl->ml_full), partner);
-      float* mref_buf = reinterpret_cast<float*>(data + C::kMrefOff);
+      volatile uint64_t* pub = reinterpret_cast<volatile uint64_t*>(data + C::kPubOff);
       const int rr = g * kRows + r;
       const bool real = rr < p.R;  // rows past H * q_len are padding: nothing of theirs is sent
       const PSlots ps(kF8, p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
@@ -916,27 +917,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (t0 + t < nvis) m4[t & 3] = fmaxf(m4[t & 3], MLA_S(t));
           }
           const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;
-          // running max after page j - 1 (a unit starts from scratch); the
-          // wait is made on every page so the chain of hand-offs stays strict
-          float m_prev = kMinusBig;
-          if (j > 0) {
-            const uint32_t jp = j - 1;
-            if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->hb[jp & 1]), (jp >> 1) & 1, abort, p.timeout_ns)) {
-              ok = false;
-              why = kWaitHandoff;
-              break;
-            }
-            if (pg != u.p0) m_prev = mref_buf[(jp & 1) * kRows + r];
+          // reference: the highest known for the row in this unit (this
+          // group's or a published one), raised to the page max when that
+          // exceeds it by more than the threshold (P then stays <= 2^thr)
+          const uint32_t tag = un + 1;
+          float m_ref = m_run;
+          {
+            const uint64_t pv = pub[r];
+            if (static_cast<uint32_t>(pv >> 32) == tag) m_ref = fmaxf(m_ref, __uint_as_float(static_cast<uint32_t>(pv)));
           }
-          const bool first = pg == u.p0;  // O is overwritten on a unit's first page
-          float m_ref = m_prev, alpha = 1.f;
-          if (mx > m_prev + SoftmaxCfg<kF8>::kThreshold) {
-            alpha = first ? 0.f : ex2_approx(m_prev - mx);
+          if (mx > m_ref + SoftmaxCfg<kF8>::kThreshold) {
             m_ref = mx;
+            pub[r] = (static_cast<uint64_t>(tag) << 32) | __float_as_uint(mx);
           }
-          mref_buf[(j & 1) * kRows + r] = m_ref;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctrl->hb[j & 1]));
           if (r == 0) MLA_TRACE_POINT(0, 8, j);
           l *= ex2_approx(m_run - m_ref);  // m_run <= m_ref: the partial sum moves to the new frame
           m_run = m_ref;
@@ -951,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (r == 0) MLA_TRACE_POINT(0, 4, j);
           // P (swizzled for the MMA) is computed 16 bytes at a time and each
           // chunk goes straight into the O CTA's shared memory, completing
-          // bytes on its p_full barrier; then the row's alpha
+          // bytes on its p_full barrier; then the row's reference
           const float nm = SoftmaxCfg<kF8>::kShift - m_ref;  // P = 2^(s * c2 - m_ref + shift)
           const uint32_t bar = mapa(smem_u32(&ctrl->p_full[ps_slot]), partner);
           const uint32_t prow = p_remote + ps_slot * ps.stride + (r >> 3) * C::kPSbo + (r & 7) * 16;
@@ -996,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
 #undef MLA_S
-          if (real) st_async_b32(alpha_remote + (ps_slot * ps.arows + r) * 4, __float_as_uint(alpha), bar);
+          if (real) st_async_b32(ref_remote + (ps_slot * ps.arows + r) * 4, __float_as_uint(m_ref), bar);
           l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
           if (r == 0) MLA_TRACE_POINT(0, 5, j);
         }
@@ -1034,7 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0, un = 0;
       bool ok = true;
       int why = 0;
-      // the S CTA sends the P rows (and alphas) of real query rows only
+      // the S CTA sends the P rows (and references) of real query rows only
       const uint32_t ptx = static_cast<uint32_t>(rows_real) * C::kPTxRow;
       if (lane == 0) {  // arm the P barriers of the first pages (bytes may land before or after)
         for (int i = 0; i < ps.n; ++i) mbar_expect_tx(smem_u32(&ctrl->p_full[i]), ptx);
@@ -1146,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tcols = tmem + lane_base + half * 256;
       const bool real = g * kRows + r < p.R;
-      const float* alpha_buf = reinterpret_cast<const float*>(data + C::kAlphaOff);
+      const float* ref_buf = reinterpret_cast<const float*>(data + C::kRefOff);
       const uint32_t ml_remote = mapa(smem_u32(data + C::kMlOff), partner);
       const uint32_t mlempty_remote = mapa(smem_u32(&ctrl->ml_empty), partner);
       UnitIter it;
@@ -1156,6 +1149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int why = 0;
       while (ok && it.next(u)) {
+        // O's frame for row r in this unit: O = sum_j P_j V_j * 2^(ref_j - F)
+        float F = kMinusBig;
         for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
           const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
           if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->p_full[pb]), (j / static_cast<uint32_t>(ps.n)) & 1, abort,
@@ -1165,9 +1160,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (r == 0 && half == 0) MLA_TRACE_POINT(1, 4, j);
-          // padding rows receive no alpha (their O rows are never stored)
-          const float a = real ? alpha_buf[pb * ps.arows + r] : 1.f;
-          if (pg != u.p0 && __any_sync(0xffffffffu, a != 1.f)) {
+          // the reference P_j was computed against (padding rows receive
+          // none: their O rows are never stored).  A unit's first page sets
+          // the frame (O is overwritten); a higher reference rescales O, a
+          // lower one scales P_j down in place before its PV
+          const float rj = real ? ref_buf[pb * ps.arows + r] : F;
+          const bool first = pg == u.p0;
+          float a = 1.f;
+          if (first) {
+            F = rj;
+          } else if (rj > F) {
+            a = ex2_approx(F - rj);
+            F = rj;
+          } else if (rj < F) {
+            const float f = ex2_approx(rj - F);
+            uint8_t* prow = data + C::kPOff + pb * ps.stride + (r >> 3) * C::kPSbo + (r & 7) * 16;
+            constexpr int kHalfChunks = C::kPChunks / 2;
+#pragma unroll
+            for (int c = half * kHalfChunks; c < (half + 1) * kHalfChunks; ++c) {
+              uint4* q = reinterpret_cast<uint4*>(prow + c * C::kPLbo);
+              uint4 v = *q;
+              uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if constexpr (!kF8) {
+                  float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+                  __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
+                  w[e] = *reinterpret_cast<uint32_t*>(&y);
+                } else {
+                  const __nv_fp8x2_storage_t lo = static_cast<__nv_fp8x2_storage_t>(w[e] & 0xFFFFu);
+                  const __nv_fp8x2_storage_t hi = static_cast<__nv_fp8x2_storage_t>(w[e] >> 16);
+                  const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
+                  const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+                  const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&hl));
+                  const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hh));
+                  const __nv_fp8x2_storage_t nl =
+                      __nv_cvt_float2_to_fp8x2(make_float2(fl.x * f, fl.y * f), __NV_SATFINITE, __NV_E4M3);
+                  const __nv_fp8x2_storage_t nh =
+                      __nv_cvt_float2_to_fp8x2(make_float2(fh.x * f, fh.y * f), __NV_SATFINITE, __NV_E4M3);
+                  w[e] = static_cast<uint32_t>(nl) | (static_cast<uint32_t>(nh) << 16);
+                }
+              }
+              *q = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_cta();  // the MMA (async proxy) reads P after these stores
+          }
+          if (!first && __any_sync(0xffffffffu, a != 1.f)) {
             // wait until PV of the previous page has landed in O, then rescale
             const uint32_t jp = j - 1;
             const uint32_t np = static_cast<uint32_t>(ps.n);
@@ -1208,13 +1246,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // the two softmax groups' (frame, partial sum); O is in the frame of
-        // the later one, which is the larger (the running max never drops)
+        // the two softmax groups' (frame, partial sum), brought to O's frame F
+        // (every group's last reference was sent with a page, so it is <= F)
         const float m0 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r));
         const float l0 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 4));
         const float m1 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 8));
         const float l1 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 12));
-        const float m_log2 = fmaxf(m0, m1);
+        const float m_log2 = F;
         const float l = l0 * ex2_approx(m0 - m_log2) + l1 * ex2_approx(m1 - m_log2);
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mlempty_remote);
