@@ -114,8 +114,9 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = make_idesc(kF8, 128, 64, false, false);
   static constexpr uint32_t kIdescPV = make_idesc(kF8, 128, 256, false, true);
   static constexpr int kMlOff = kNStS * kSlotS;          // S CTA: (m0, l0, m1, l1)[128], one pair per group
-  static constexpr int kPubOff = kMlOff + 4 * kRows * 4;  // S CTA: published row references [128] (unit tag, value)
-  static constexpr int kDataS = kPubOff + kRows * 8;
+  // S CTA: the row references of the last 4 pages [4][128] (page tag, value)
+  static constexpr int kPubOff = kMlOff + 4 * kRows * 4;
+  static constexpr int kDataS = kPubOff + 4 * kRows * 8;
   // O CTA: P slots first (a slot's padding rows read on into what follows,
   // which must be shared memory of this CTA), then the c_kv ring, then the
   // row references that come with each P
@@ -359,7 +360,7 @@ struct UnitIter {
 enum WaitTag : int {
   kWaitProdEmptyS = 1, kWaitProdEmptyO, kWaitQFull, kWaitKvFullS, kWaitSEmpty, kWaitSFull, kWaitPEmptyS,
   kWaitMlEmpty, kWaitKvFullO, kWaitPFullO, kWaitOEmpty, kWaitRescDone, kWaitPFullCorr, kWaitPvPrev,
-  kWaitOFull, kWaitMlFull, kWaitSPrevUnit, kWaitPvReady, kWaitPvTaken, kWaitQEntry
+  kWaitOFull, kWaitMlFull, kWaitSPrevUnit, kWaitPvReady, kWaitPvTaken, kWaitQEntry, kWaitPub
 };
 
 __device__ __forceinline__ void raise_timeout(const Params& p, Ctrl* ctrl, uint32_t partner_rank, int tag,
@@ -712,8 +713,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&ctrl->tmem_base), 512);
     tmem_relinquish();
   }
-  if (role_s && threadIdx.x >= 128 && threadIdx.x < 256)  // published references: no unit yet
-    reinterpret_cast<uint64_t*>(data + C::kPubOff)[threadIdx.x - 128] = 0ull;
+  if (role_s && threadIdx.x >= 128)  // page references: no page yet
+    for (int i = threadIdx.x - 128; i < 4 * kRows; i += blockDim.x - 128)
+      reinterpret_cast<uint64_t*>(data + C::kPubOff)[i] = 0ull;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -815,9 +817,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- softmax: group gg (warps 4-7: 0, warps 8-11: 1) takes the pages
       // j with j % 2 == gg; its thread r owns query row r.  P of a page is
       // computed against a reference (a running max of the row) that is
-      // sent with it; the O CTA brings every page to one frame.  Handlers
-      // share references through a published value per row (tagged with the
-      // unit), so pages rarely disagree; nothing waits for another page.
+      // sent with it; the O CTA brings every page to one frame.  A page's
+      // reference is the previous page's, raised to the page max when that
+      // exceeds it by more than a threshold; each page publishes its own.
+      // So references are a function of the data alone (results do not
+      // depend on timing) and never fall within a unit; a page waits only
+      // for the previous page's row max, not for its P.
       // Each group keeps its partial sum in the frame of its latest reference.
       const int r = (warp & 3) * 32 + lane;
       const int gg = (warp - 4) >> 2;
@@ -917,19 +922,31 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (t0 + t < nvis) m4[t & 3] = fmaxf(m4[t & 3], MLA_S(t));
           }
           const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;
-          // reference: the highest known for the row in this unit (this
-          // group's or a published one), raised to the page max when that
-          // exceeds it by more than the threshold (P then stays <= 2^thr)
-          const uint32_t tag = un + 1;
+          // reference: the previous page's of the unit (entry (j - 1) % 4,
+          // tagged j), raised to the page max when that exceeds it by more
+          // than the threshold (P then stays <= 2^thr); published in entry
+          // j % 4 with tag j + 1.  The entry is rewritten by page j + 3 only,
+          // whose reference needs this page's, so no entry is overwritten
+          // before it was read.
           float m_ref = m_run;
-          {
-            const uint64_t pv = pub[r];
-            if (static_cast<uint32_t>(pv >> 32) == tag) m_ref = fmaxf(m_ref, __uint_as_float(static_cast<uint32_t>(pv)));
+          if (pg != u.p0) {
+            volatile uint64_t* pe = pub + ((j - 1u) & 3u) * kRows + r;
+            uint64_t pv = *pe;
+            if (static_cast<uint32_t>(pv >> 32) != j) {
+              const uint64_t t_start = globaltimer_ns();
+              while (static_cast<uint32_t>((pv = *pe) >> 32) != j) {
+                if (*abort || globaltimer_ns() - t_start > p.timeout_ns) break;
+              }
+            }
+            if (__any_sync(0xffffffffu, static_cast<uint32_t>(pv >> 32) != j)) {
+              ok = false;
+              why = kWaitPub;
+              break;
+            }
+            m_ref = fmaxf(m_ref, __uint_as_float(static_cast<uint32_t>(pv)));
           }
-          if (mx > m_ref + SoftmaxCfg<kF8>::kThreshold) {
-            m_ref = mx;
-            pub[r] = (static_cast<uint64_t>(tag) << 32) | __float_as_uint(mx);
-          }
+          if (mx > m_ref + SoftmaxCfg<kF8>::kThreshold) m_ref = mx;
+          pub[(j & 3u) * kRows + r] = (static_cast<uint64_t>(j + 1u) << 32) | __float_as_uint(m_ref);
           if (r == 0) MLA_TRACE_POINT(0, 8, j);
           l *= ex2_approx(m_run - m_ref);  // m_run <= m_ref: the partial sum moves to the new frame
           m_run = m_ref;
