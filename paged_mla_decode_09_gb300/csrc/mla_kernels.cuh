@@ -26,7 +26,7 @@
 // Every barrier below is used so that its completer can never run two phases
 // ahead of a waiter (parity waits would then miss a phase).  Where a chain
 // of barriers does not already guarantee that, the barrier is split per
-// P slot (p_full, p_empty, resc_done).
+// P slot (p_full, p_empty).
 #pragma once
 
 #include <cstdint>
@@ -63,14 +63,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy output rescale: O is rescaled only when a row's running max grows by
 // more than the threshold (log2 units).  P is computed relative to the stale
-// max, times 2^shift, so that it never exceeds 2^8 (bf16: threshold 8, no
-// shift).  For e4m3, P is shifted up by 2^5 with threshold 3: the bulk of
-// the probability mass then sits in e4m3's normal range instead of its
-// subnormals; the shift cancels in out = O / l and is removed from the lse.
+// max, times 2^shift, so that it never exceeds 2^(threshold + shift) (bf16:
+// threshold 8, no shift).  For e4m3, threshold 5 and shift 3 keep P at most
+// 2^8 (e4m3's largest finite value is 448) while the bulk of the
+// probability mass sits in its normal range rather than its subnormals; an
+// integral shift keeps the P of a row's max key (2^shift) exact.
+// Every page on which one of the block's rows crosses the threshold stalls
+// PV for an O rescale: over a long sequence of Gaussian-like scores one of
+// 128 rows crosses 3 on most pages, 5 on few.  The shift cancels in
+// out = O / l and is removed from the lse.
 template <bool kF8>
 struct SoftmaxCfg {
-  static constexpr float kThreshold = kF8 ? 3.0f : 8.0f;
-  static constexpr float kShift = kF8 ? 5.0f : 0.0f;
+  static constexpr float kThreshold = kF8 ? 5.0f : 8.0f;
+  static constexpr float kShift = kF8 ? 3.0f : 0.0f;
+  static_assert(kThreshold + kShift <= 8.f, "P must stay below e4m3's largest finite value");
 };
 constexpr float kMinusBig = -1.0e30f;      // running-max sentinel (finite, so exp2 never sees inf - inf)
 
@@ -125,12 +131,15 @@ struct Cfg {
   static constexpr int kRingOffO = kPOff + kPRegion;
   static constexpr int kRefOff = kRingOffO + kNStO * kSlotO;
   static constexpr int kRefBytes = kF8 ? 3 * kRows * 4 : 2 * kRows * 4;
-  static constexpr int kDataO = kRefOff + kRefBytes;
+  static constexpr int kFlagOff = kRefOff + kRefBytes;  // per P slot: one word per softmax warp (rows that rose)
+  static constexpr int kDataO = kFlagOff + 4 * 16;
   static constexpr int kData = kDataS > kDataO ? kDataS : kDataO;
   // dynamic smem = alignment slack + 1024-aligned data + control block
   static constexpr int kSmem = 1024 + kData + kCtrlBytes;
-  // bytes the S CTA sends per page and real query row: P row + its reference
+  // bytes the S CTA sends per page: per real query row its P row and O
+  // scale factor, and one flag word per softmax warp
   static constexpr uint32_t kPTxRow = kPRow + 4;
+  static constexpr uint32_t kPTxFlags = 4 * 4;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -164,13 +173,15 @@ struct __align__(8) Ctrl {
   uint64_t p_empty[kMaxPSlots];
   uint64_t o_full;
   uint64_t o_empty;
-  uint64_t resc_done[kMaxPSlots];
+  uint64_t resc_req;   // O CTA: page resc_page needs O rescaled (waiter -> correction warps)
+  uint64_t resc_done;  // O CTA: the correction warps rescaled O
   uint64_t ml_full;
   uint64_t ml_empty;
   uint64_t pv_ready;  // O CTA: page j is ready for PV (waiter warp -> MMA warp)
   uint64_t pv_taken;  // O CTA: the MMA warp took page j (keeps the waiter one page ahead at most)
   uint64_t drain;
   uint32_t tmem_base;
+  uint32_t resc_page;
   int abort;
 };
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
@@ -693,8 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kMaxPSlots; ++i) {
       mbar_init(smem_u32(&ctrl->p_full[i]), 1);  // one arm (expect_tx) by the O MMA warp + P bytes
       mbar_init(smem_u32(&ctrl->p_empty[i]), 1);
-      mbar_init(smem_u32(&ctrl->resc_done[i]), kRowWarps);
     }
+    mbar_init(smem_u32(&ctrl->resc_req), 1);
+    mbar_init(smem_u32(&ctrl->resc_done), kRowWarps);
     mbar_init(smem_u32(&ctrl->o_full), 1);
     mbar_init(smem_u32(&ctrl->o_empty), kRowWarps);
     mbar_init(smem_u32(&ctrl->ml_full), kRowWarps);
@@ -829,6 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t p_remote = mapa(smem_u32(data + C::kPOff), partner);
       const uint32_t ref_remote = mapa(smem_u32(data + C::kRefOff), partner);
+      const uint32_t flag_remote = mapa(smem_u32(data + C::kFlagOff), partner);
       const uint32_t mlfull_remote = mapa(smem_u32(&ctrl->ml_full), partner);
       volatile uint64_t* pub = reinterpret_cast<volatile uint64_t*>(data + C::kPubOff);
       const int rr = g * kRows + r;
@@ -929,6 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // whose reference needs this page's, so no entry is overwritten
           // before it was read.
           float m_ref = m_run;
+          float m_prev = kMinusBig;  // the previous page's reference: O's frame before this page
           if (pg != u.p0) {
             volatile uint64_t* pe = pub + ((j - 1u) & 3u) * kRows + r;
             uint64_t pv = *pe;
@@ -943,10 +957,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               why = kWaitPub;
               break;
             }
-            m_ref = fmaxf(m_ref, __uint_as_float(static_cast<uint32_t>(pv)));
+            m_prev = __uint_as_float(static_cast<uint32_t>(pv));
+            m_ref = fmaxf(m_ref, m_prev);
           }
           if (mx > m_ref + SoftmaxCfg<kF8>::kThreshold) m_ref = mx;
           pub[(j & 3u) * kRows + r] = (static_cast<uint64_t>(j + 1u) << 32) | __float_as_uint(m_ref);
+          // O holds the earlier pages in the frame m_prev: when the reference
+          // rose, O is scaled by o_scale before this page's PV (a unit's
+          // first page sets the frame: its PV overwrites O)
+          const bool rose = pg != u.p0 && m_ref > m_prev;
+          const float o_scale = rose ? ex2_approx(m_prev - m_ref) : 1.f;
+          const uint32_t rose_mask = __ballot_sync(0xffffffffu, rose && real);
           if (r == 0) MLA_TRACE_POINT(0, 8, j);
           l *= ex2_approx(m_run - m_ref);  // m_run <= m_ref: the partial sum moves to the new frame
           m_run = m_ref;
@@ -1006,7 +1027,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
 #undef MLA_S
-          if (real) st_async_b32(ref_remote + (ps_slot * ps.arows + r) * 4, __float_as_uint(m_ref), bar);
+          if (real) st_async_b32(ref_remote + (ps_slot * ps.arows + r) * 4, __float_as_uint(o_scale), bar);
+          if (lane == 0) st_async_b32(flag_remote + (ps_slot * 4 + (warp & 3)) * 4, rose_mask, bar);
           l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
           if (r == 0) MLA_TRACE_POINT(0, 5, j);
         }
@@ -1044,8 +1066,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0, un = 0;
       bool ok = true;
       int why = 0;
-      // the S CTA sends the P rows (and references) of real query rows only
-      const uint32_t ptx = static_cast<uint32_t>(rows_real) * C::kPTxRow;
+      // the S CTA sends the P rows (and O scale factors) of real query rows
+      // only, and every softmax warp's flag word
+      const uint32_t ptx = static_cast<uint32_t>(rows_real) * C::kPTxRow + C::kPTxFlags;
+      const volatile uint32_t* flag_buf = reinterpret_cast<const volatile uint32_t*>(data + C::kFlagOff);
+      uint32_t nreq = 0;  // rescale requests handed to the correction warps
       if (lane == 0) {  // arm the P barriers of the first pages (bytes may land before or after)
         for (int i = 0; i < ps.n; ++i) mbar_expect_tx(smem_u32(&ctrl->p_full[i]), ptx);
       }
@@ -1063,15 +1088,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             why = kWaitOEmpty;
             break;
           }
-          {  // PV(j - 1) taken, c_kv landed, P arrived, rescale acknowledged
+          {  // PV(j - 1) taken, c_kv landed, P arrived
             const uint32_t bars[4] = {j > 0 ? smem_u32(&ctrl->pv_taken) : 0u, smem_u32(&ctrl->kv_full[st]),
-                                      smem_u32(&ctrl->p_full[pb]), smem_u32(&ctrl->resc_done[pb])};
-            const uint32_t pars[4] = {(j - 1) & 1, kph, pph, pph};
+                                      smem_u32(&ctrl->p_full[pb]), 0u};
+            const uint32_t pars[4] = {(j - 1) & 1, kph, pph, 0u};
             if (!mbar_wait4_warp(bars, pars, abort, p.timeout_ns)) {
               ok = false;
               why = kWaitPFullO;
               break;
             }
+          }
+          // a page on which some row's reference rose needs O rescaled first
+          // (after PV(j - 1)): the correction warps do it and acknowledge.
+          // PV(j) waits for that, so one request at most is outstanding.
+          const uint32_t fw = lane < 4 ? flag_buf[pb * 4 + lane] : 0u;
+          if (__any_sync(0xffffffffu, fw != 0u)) {
+            if (lane == 0) {
+              ctrl->resc_page = j;
+              mbar_arrive(smem_u32(&ctrl->resc_req));  // release: resc_page is seen with the phase
+            }
+            if (!mbar_wait_warp(smem_u32(&ctrl->resc_done), nreq & 1, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitRescDone;
+              break;
+            }
+            ++nreq;
           }
           // phase for page j done: arm this P slot for page j + ps.n.  Its
           // bytes cannot come earlier: the S CTA sends them only after PV(j)
@@ -1156,82 +1197,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tcols = tmem + lane_base + half * 256;
       const bool real = g * kRows + r < p.R;
-      const float* ref_buf = reinterpret_cast<const float*>(data + C::kRefOff);
+      const float* scale_buf = reinterpret_cast<const float*>(data + C::kRefOff);
       const uint32_t ml_remote = mapa(smem_u32(data + C::kMlOff), partner);
       const uint32_t mlempty_remote = mapa(smem_u32(&ctrl->ml_empty), partner);
       UnitIter it;
       it.init(p, cid);
       Unit u;
-      uint32_t j = 0, un = 0;
+      uint32_t j = 0, un = 0, nreq = 0;
       bool ok = true;
       int why = 0;
       while (ok && it.next(u)) {
-        // O's frame for row r in this unit: O = sum_j P_j V_j * 2^(ref_j - F)
-        float F = kMinusBig;
-        for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
-          const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
-          if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->p_full[pb]), (j / static_cast<uint32_t>(ps.n)) & 1, abort,
-                              p.timeout_ns)) {
+        // serve this unit's rescale requests until its last PV has landed
+        // (a pending request holds back a PV of the unit, so o_full cannot
+        // complete while one is pending; the next unit's first PV waits for
+        // this unit's epilogue)
+        const uint64_t t_unit = globaltimer_ns();
+        while (true) {
+          bool req = false, done = false;
+          while (true) {
+            req = mbar_try_wait(smem_u32(&ctrl->resc_req), nreq & 1);
+            done = !req && mbar_try_wait(smem_u32(&ctrl->o_full), un & 1);
+            if (__any_sync(0xffffffffu, req || done)) break;
+            if (*abort || globaltimer_ns() - t_unit > p.timeout_ns) break;
+            __nanosleep(32);
+          }
+          req = __any_sync(0xffffffffu, req);
+          done = !req && __any_sync(0xffffffffu, done);
+          if (!req && !done) {
             ok = false;
-            why = kWaitPFullCorr;
+            why = kWaitOFull;
             break;
           }
-          if (r == 0 && half == 0) MLA_TRACE_POINT(1, 4, j);
-          // the reference P_j was computed against (padding rows receive
-          // none: their O rows are never stored).  A unit's first page sets
-          // the frame (O is overwritten); a higher reference rescales O, a
-          // lower one scales P_j down in place before its PV
-          const float rj = real ? ref_buf[pb * ps.arows + r] : F;
-          const bool first = pg == u.p0;
-          float a = 1.f;
-          if (first) {
-            F = rj;
-          } else if (rj > F) {
-            a = ex2_approx(F - rj);
-            F = rj;
-          } else if (rj < F) {
-            const float f = ex2_approx(rj - F);
-            uint8_t* prow = data + C::kPOff + pb * ps.stride + (r >> 3) * C::kPSbo + (r & 7) * 16;
-            constexpr int kHalfChunks = C::kPChunks / 2;
-#pragma unroll
-            for (int c = half * kHalfChunks; c < (half + 1) * kHalfChunks; ++c) {
-              uint4* q = reinterpret_cast<uint4*>(prow + c * C::kPLbo);
-              uint4 v = *q;
-              uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                if constexpr (!kF8) {
-                  float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-                  __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
-                  w[e] = *reinterpret_cast<uint32_t*>(&y);
-                } else {
-                  const __nv_fp8x2_storage_t lo = static_cast<__nv_fp8x2_storage_t>(w[e] & 0xFFFFu);
-                  const __nv_fp8x2_storage_t hi = static_cast<__nv_fp8x2_storage_t>(w[e] >> 16);
-                  const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
-                  const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
-                  const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&hl));
-                  const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hh));
-                  const __nv_fp8x2_storage_t nl =
-                      __nv_cvt_float2_to_fp8x2(make_float2(fl.x * f, fl.y * f), __NV_SATFINITE, __NV_E4M3);
-                  const __nv_fp8x2_storage_t nh =
-                      __nv_cvt_float2_to_fp8x2(make_float2(fh.x * f, fh.y * f), __NV_SATFINITE, __NV_E4M3);
-                  w[e] = static_cast<uint32_t>(nl) | (static_cast<uint32_t>(nh) << 16);
-                }
-              }
-              *q = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            fence_proxy_async_cta();  // the MMA (async proxy) reads P after these stores
+          if (done) break;
+          // page jr raised some rows' references: O *= 2^(old - new) once
+          // PV(jr - 1), the last one issued, has landed
+          const uint32_t jr = *reinterpret_cast<volatile uint32_t*>(&ctrl->resc_page);
+          const uint32_t np = static_cast<uint32_t>(ps.n);
+          if (r == 0 && half == 0) MLA_TRACE_POINT(1, 4, jr);
+          const float a = real ? scale_buf[(jr % np) * ps.arows + r] : 1.f;
+          if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->p_empty[(jr - 1) % np]), ((jr - 1) / np) & 1, abort,
+                                           p.timeout_ns)) {
+            ok = false;
+            why = kWaitPvPrev;
+            break;
           }
-          if (!first && __any_sync(0xffffffffu, a != 1.f)) {
-            // wait until PV of the previous page has landed in O, then rescale
-            const uint32_t jp = j - 1;
-            const uint32_t np = static_cast<uint32_t>(ps.n);
-            if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->p_empty[jp % np]), (jp / np) & 1, abort, p.timeout_ns)) {
-              ok = false;
-              why = kWaitPvPrev;
-              break;
-            }
-            tc_fence_after();
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, a != 1.f)) {
             for (int c = 0; c < 256; c += 16) {
               uint32_t v[16];
               tmem_ld16(tcols + c, v);
@@ -1242,20 +1253,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
           }
-          // acknowledge page j (rescaled or not); PV of page j waits for this
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctrl->resc_done[pb]));
-          if (r == 0 && half == 0) MLA_TRACE_POINT(1, 5, j);
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->resc_done));
+          if (r == 0 && half == 0) MLA_TRACE_POINT(1, 5, jr);
+          ++nreq;
         }
         if (!ok) break;
+        j += static_cast<uint32_t>(u.p1 - u.p0);
         // epilogue for this unit
         if (r == 0 && half == 0) MLA_TRACE_POINT(1, 13, un);
-        if (!mbar_wait_warp<false, true>(smem_u32(&ctrl->o_full), un & 1, abort, p.timeout_ns)) {
-          ok = false;
-          why = kWaitOFull;
-          break;
-        }
         if (r == 0 && half == 0) MLA_TRACE_POINT(1, 14, un);
         if (!mbar_wait_warp<true, true>(smem_u32(&ctrl->ml_full), un & 1, abort, p.timeout_ns)) {
           ok = false;
@@ -1263,13 +1270,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // the two softmax groups' (frame, partial sum), brought to O's frame F
-        // (every group's last reference was sent with a page, so it is <= F)
+        // the two softmax groups' (frame, partial sum), brought to O's frame:
+        // references never fall within a unit, so O ends in the frame of the
+        // last page's reference, the higher of the two groups' last ones
         const float m0 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r));
         const float l0 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 4));
         const float m1 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 8));
         const float l1 = __uint_as_float(ld_cluster_u32(ml_remote + 16 * r + 12));
-        const float m_log2 = F;
+        const float m_log2 = fmaxf(m0, m1);
         const float l = l0 * ex2_approx(m0 - m_log2) + l1 * ex2_approx(m1 - m_log2);
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mlempty_remote);
