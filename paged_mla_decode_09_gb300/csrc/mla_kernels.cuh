@@ -89,7 +89,7 @@ struct Cfg {
   static constexpr int kSlotS = kNBoxLat * kBox + kPeBytes;
   static constexpr int kSlotO = kNBoxLat * kBox;
   static constexpr int kNStS = kF8 ? 6 : 3;
-  static constexpr int kNStO = kF8 ? 6 : 3;
+  static constexpr int kNStO = kF8 ? 5 : 3;
   // One copy per page (measured on GB300: three 24 KB copies per page
   // instead of one 72 KB copy raise the copy latency about threefold).
   static constexpr int kBoxesPartS = kF8 ? 4 : 9;   // boxes of the c_kv / whole-row map per copy
@@ -109,6 +109,12 @@ struct Cfg {
   static constexpr uint32_t kPLbo = 128;                // next core matrix along K
   static constexpr uint32_t kPSbo = kF8 ? 512 : 1024;   // next 8-row group
   static constexpr int kPChunks = kF8 ? 4 : 8;          // 16-byte chunks per P row
+  // e4m3 P is sent as two terms hi + lo (hi = e4m3(p), lo = e4m3(p - hi)),
+  // two 8 KB tiles of one slot, both multiplied by the same V page: one
+  // e4m3 term alone (3 mantissa bits) moves a row's weights by a few
+  // percent when it sees only a handful of keys
+  static constexpr int kPTerms = kF8 ? 2 : 1;
+  static constexpr uint32_t kPTermBytes = kRows * kPage;  // e4m3: 8 KB
   static constexpr int kPvKSteps = kF8 ? 2 : 4;         // K = 64 tokens in steps of 32 (e4m3) / 16 (bf16)
   static constexpr int kVKStepBytes = kF8 ? 4096 : 2048;
   static constexpr int kVBoxesHalf = kF8 ? 2 : 4;       // boxes covering 256 output columns
@@ -127,10 +133,10 @@ struct Cfg {
   // which must be shared memory of this CTA), then the c_kv ring, then the
   // row references that come with each P
   static constexpr int kPOff = 0;
-  static constexpr int kPRegion = kF8 ? 3 * 8192 : 4 * 8192;
+  static constexpr int kPRegion = kF8 ? 3 * 16384 : 4 * 8192;
   static constexpr int kRingOffO = kPOff + kPRegion;
   static constexpr int kRefOff = kRingOffO + kNStO * kSlotO;
-  static constexpr int kRefBytes = kF8 ? 3 * kRows * 4 : 2 * kRows * 4;
+  static constexpr int kRefBytes = (kF8 ? 3 : 2) * kRows * 4;
   static constexpr int kFlagOff = kRefOff + kRefBytes;  // per P slot: one word per softmax warp (rows that rose)
   static constexpr int kDataO = kFlagOff + 4 * 16;
   static constexpr int kData = kDataS > kDataO ? kDataS : kDataO;
@@ -138,7 +144,7 @@ struct Cfg {
   static constexpr int kSmem = 1024 + kData + kCtrlBytes;
   // bytes the S CTA sends per page: per real query row its P row and O
   // scale factor, and one flag word per softmax warp
-  static constexpr uint32_t kPTxRow = kPRow + 4;
+  static constexpr uint32_t kPTxRow = kPRow * kPTerms + 4;
   static constexpr uint32_t kPTxFlags = 4 * 4;
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -146,14 +152,15 @@ struct Cfg {
 // P slots of a row block in the O CTA.  bf16: a P row is 128 bytes; with at
 // most 64 real rows a slot needs only 8 KB (the MMA's rows 64-127 read the
 // next 8 KB, whose results land in O rows that are never stored), so the
-// 32 KB region holds 4 slots, else 2 of 16 KB.  e4m3: 3 slots of 8 KB.
+// 32 KB region holds 4 slots, else 2 of 16 KB.  e4m3: 3 slots of 16 KB,
+// each the hi and the lo tile (8 KB each) of one page.
 struct PSlots {
   int n;            // slots
   uint32_t stride;  // bytes from one slot to the next
   int arows;        // reference entries per slot
   __device__ PSlots(bool f8, int rows_real) {
     if (f8) {
-      n = 3; stride = 8192; arows = kRows;
+      n = 3; stride = 16384; arows = kRows;  // hi and lo tiles
     } else if (rows_real <= 64) {
       n = 4; stride = 8192; arows = 64;
     } else {
@@ -1007,23 +1014,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {  // keys 16c .. 16c + 15
-              uint32_t w[4];
+              uint32_t wh[4], wl[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const int t = 16 * c + 4 * k;
-                const __nv_fp8x2_storage_t lo =
-                    __nv_cvt_float2_to_fp8x2(make_float2(prob(t), prob(t + 1)), __NV_SATFINITE, __NV_E4M3);
-                const __nv_fp8x2_storage_t hi =
-                    __nv_cvt_float2_to_fp8x2(make_float2(prob(t + 2), prob(t + 3)), __NV_SATFINITE, __NV_E4M3);
-                // l sums the e4m3-rounded P actually multiplied into O
-                const __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
-                const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
-                const float2 fl = __half22float2(*reinterpret_cast<const __half2*>(&hl));
-                const float2 fh = __half22float2(*reinterpret_cast<const __half2*>(&hh));
-                s4[k] += (fl.x + fl.y) + (fh.x + fh.y);
-                w[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+                const float2 pa = make_float2(prob(t), prob(t + 1));
+                const float2 pb = make_float2(prob(t + 2), prob(t + 3));
+                // in f16 (e4m3 values convert to it exactly, and the residual
+                // of an f16 value by its e4m3 rounding is exact in f16)
+                const __half2 fa = __float22half2_rn(pa);
+                const __half2 fb = __float22half2_rn(pb);
+                const __nv_fp8x2_storage_t ha =
+                    __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&fa), __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t hb =
+                    __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&fb), __NV_SATFINITE, __NV_E4M3);
+                const __half2_raw xa = __nv_cvt_fp8x2_to_halfraw2(ha, __NV_E4M3);
+                const __half2_raw xb = __nv_cvt_fp8x2_to_halfraw2(hb, __NV_E4M3);
+                const __half2 ra = __hsub2(fa, *reinterpret_cast<const __half2*>(&xa));
+                const __half2 rb = __hsub2(fb, *reinterpret_cast<const __half2*>(&xb));
+                const __nv_fp8x2_storage_t la =
+                    __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&ra), __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t lb =
+                    __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&rb), __NV_SATFINITE, __NV_E4M3);
+                // hi + lo equals p to about 2^-8 relative
+                s4[k] += (pa.x + pa.y) + (pb.x + pb.y);
+                wh[k] = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
+                wl[k] = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 16);
               }
-              if (real) st_async_v4(prow + c * C::kPLbo, make_uint4(w[0], w[1], w[2], w[3]), bar);
+              if (real) {
+                st_async_v4(prow + c * C::kPLbo, make_uint4(wh[0], wh[1], wh[2], wh[3]), bar);
+                st_async_v4(prow + C::kPTermBytes + c * C::kPLbo, make_uint4(wl[0], wl[1], wl[2], wl[3]), bar);
+              }
             }
           }
 #undef MLA_S
@@ -1164,16 +1185,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_cta();
           tc_fence_after();
           {  // the whole warp issues; one elected lane executes
-            const uint64_t dp = smem_desc(smem_u32(pbuf + pb * ps.stride), C::kPLbo, C::kPSbo, C::kPSwz);
             const uint64_t dv = smem_desc(smem_u32(ring + st * C::kSlotO), C::kBox, 1024, kSwizzle128B);
-            // O[:, 256h .. 256h + 255] += P V[:, 256h ..]
+            // O[:, 256h .. 256h + 255] += P V[:, 256h ..], for each term of P
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int tm = 0; tm < C::kPTerms; ++tm) {
+              const uint64_t dp =
+                  smem_desc(smem_u32(pbuf + pb * ps.stride + tm * C::kPTermBytes), C::kPLbo, C::kPSbo, C::kPSwz);
 #pragma unroll
-              for (int k = 0; k < C::kPvKSteps; ++k)
-                mma_ss_e<kF8>(tmem + h * 256, dp + static_cast<uint64_t>(k * (2 * C::kPLbo >> 4)),
-                              dv + static_cast<uint64_t>((h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes) >> 4),
-                              C::kIdescPV, (first && k == 0) ? 0u : 1u);
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k = 0; k < C::kPvKSteps; ++k)
+                  mma_ss_e<kF8>(tmem + h * 256, dp + static_cast<uint64_t>(k * (2 * C::kPLbo >> 4)),
+                                dv + static_cast<uint64_t>((h * C::kVBoxesHalf * C::kBox + k * C::kVKStepBytes) >> 4),
+                                C::kIdescPV, (first && tm == 0 && k == 0) ? 0u : 1u);
+            }
             mma_commit_e(smem_u32(&ctrl->kv_empty[st]));
             mma_commit_multicast_e(smem_u32(&ctrl->p_empty[pb]), mask);
             if (pg == u.p1 - 1) mma_commit_e(smem_u32(&ctrl->o_full));

@@ -17,6 +17,7 @@ kimi       64    64    1   8192 each; pool sized to the batch
 dsv3       128   128   1   floor(exp(U(ln 1024, ln 32768))); split-KV needed
 prefix     32    64    1   768 shared prefix pages + U{1024..4096} private
 fp8        256   128   2   U{4096..16384}; E4M3 cache, one fp32 scale
+verify4    64    64    4   8192 each: kimi's shape verifying 3 draft tokens
 =========  ====  ====  ==  =================================================
 
 Recipe (all integers drawn from one ``numpy.random.Generator(PCG64(seed))``
@@ -53,7 +54,7 @@ _CHUNK_PAGES = 256
 BF16_NAN = np.uint16(0x7FC0)
 E4M3_NAN = np.uint8(0x7F)
 
-CONFIG_NAMES = ("tiny", "kimi", "dsv3", "prefix", "fp8")
+CONFIG_NAMES = ("tiny", "kimi", "dsv3", "prefix", "fp8", "verify4")
 
 
 @dataclass
@@ -254,7 +255,7 @@ def default_seed(name: str) -> int:
 
 
 def make_config(name: str, seed: int | None = None, sentinel: str = "nan") -> Workload:
-    """One of the five named decode batches (default seed: default_seed(name))."""
+    """One of the named decode batches (default seed: default_seed(name))."""
     seed = default_seed(name) if seed is None else seed
     rng = np.random.Generator(np.random.PCG64(seed))
     if name == "tiny":
@@ -305,6 +306,15 @@ def make_config(name: str, seed: int | None = None, sentinel: str = "nan") -> Wo
         perm = rng.permutation(pool).astype(np.int32)
         table, _ = _tables_private(seq_lens, perm)
         return build(name, H, 2, seq_lens, table, pool, rng, seed, "fp8_e4m3", sentinel=sentinel)
+    if name == "verify4":
+        # speculative verification: the new token and 3 drafts per request,
+        # causal among themselves; 4 * 64 = 256 query rows per request
+        B, H = 64, 64
+        seq_lens = np.full(B, 8192, dtype=np.int32)
+        pool = B * 128
+        perm = rng.permutation(pool).astype(np.int32)
+        table, _ = _tables_private(seq_lens, perm)
+        return build(name, H, 4, seq_lens, table, pool, rng, seed, "bf16", sentinel=sentinel)
     raise ValueError(name)
 
 

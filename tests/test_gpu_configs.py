@@ -1,4 +1,4 @@
-"""The five named decode batches at full size, in the launch configuration the
+"""The named decode batches at full size, in the launch configuration the
 benchmark times, checked against the oracle on sampled requests (the first,
 the last and the longest) element by element, plus whole-batch properties
 (finite outputs, status word clear)."""
@@ -25,7 +25,7 @@ def _lib():
 from gpu_helpers import compare, run_gpu  # noqa: E402
 
 
-@pytest.mark.parametrize("name", ["kimi", "dsv3", "prefix", "fp8"])
+@pytest.mark.parametrize("name", ["kimi", "dsv3", "prefix", "fp8", "verify4"])
 def test_full_size_config_sampled(name):
     wl = W.make_config(name)
     out, lse, status, *_ = run_gpu(wl)

@@ -47,6 +47,13 @@ RAGGED = [
     ([5000, 1024], 64, 1, "fp8_e4m3"),
     ([64, 129, 700], 64, 1, "fp8_e4m3"),
     ([2, 65, 129, 700], 16, 2, "fp8_e4m3"),
+    # speculative verification with 2-3 drafts: 256, 192 (a 64-row second
+    # block) and 64 rows per request; q_len 16 at 16 heads fills 256 rows
+    ([4, 5, 64, 67, 700, 3000], 64, 4, "bf16"),
+    ([3, 67, 1300], 64, 3, "bf16"),
+    ([4, 100, 2100], 16, 4, "bf16"),
+    ([5, 129, 3000], 64, 4, "fp8_e4m3"),
+    ([16, 200, 1000], 16, 16, "bf16"),
 ]
 
 
@@ -130,21 +137,25 @@ def test_prefix_share_equals_copy_bit_identical():
     compare(wl, a[0], a[1], label="prefix-small")
 
 
-def test_causal_rows_match_single_position_calls():
-    wl = W.custom([300, 65, 2, 1000], num_heads=64, q_len=2, seed=12)
-    out2, lse2, st, *_ = run_gpu(wl)
+@pytest.mark.parametrize("Q", [2, 4])
+def test_causal_rows_match_single_position_calls(Q):
+    # draft position i of a q_len-Q call sees as many keys as a q_len-1 call
+    # on a sequence Q - 1 - i tokens shorter
+    wl = W.custom([300, 65, Q, 1000], num_heads=64, q_len=Q, seed=12)
+    outq, lseq, st, *_ = run_gpu(wl)
     assert st == 0
     atol, rtol = TOL["bf16"]
     from dataclasses import replace
 
-    for i, shift in ((1, 0), (0, 1)):
+    for i in range(Q):
+        shift = Q - 1 - i
         w1 = replace(wl, q_nope=np.ascontiguousarray(wl.q_nope[:, i:i + 1]),
                      q_pe=np.ascontiguousarray(wl.q_pe[:, i:i + 1]), q_len=1,
                      seq_lens=(wl.seq_lens - shift).astype(np.int32))
         o1, l1, st1, *_ = run_gpu(w1)
         assert st1 == 0
-        assert np.all(np.abs(out2[:, i] - o1[:, 0]) <= atol + rtol * np.abs(o1[:, 0]))
-        assert np.all(np.abs(lse2[:, i] - l1[:, 0]) <= atol + rtol * np.abs(l1[:, 0]))
+        assert np.all(np.abs(outq[:, i] - o1[:, 0]) <= atol + rtol * np.abs(o1[:, 0]))
+        assert np.all(np.abs(lseq[:, i] - l1[:, 0]) <= atol + rtol * np.abs(l1[:, 0]))
 
 
 def test_deterministic_and_cache_untouched():
