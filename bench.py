@@ -8,6 +8,10 @@ each, 64-token pages, bf16 latent cache).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
     python bench.py --impl reference ...   # the CPU float64 oracle instead
+    python bench.py --op kv_pack ...       # the cache write before a step
+
+``--op kv_pack``: one step = one quantise-and-scatter of a Kimi-shaped
+prefill (64 requests x 4096 new tokens) into an e4m3 cache; metric rows/s.
 
 Prints one JSON line (rank 0).  With N > 1 (torchrun, one rank per GPU)
 every rank decodes its own replica of the batch (requests are independent,
@@ -414,6 +418,174 @@ def run_ours(args):
     return 0
 
 
+KV_PACK_METRIC = "KV-pack rows/s"
+KV_PACK_UNIT = "rows/s"
+
+
+def kv_pack_oracle_rate(wl, budget_s: float):
+    """rows/s of the oracle's quantise-and-scatter on a bounded sample of
+    rows (one request's rows at a time, until the budget is spent)."""
+    import oracle
+
+    B, n_new, _ = wl.rows_bits.shape
+    rows, t_total = 0, 0.0
+    cache = np.zeros((wl.num_pages, 64, 576), dtype=np.uint8)
+    per = 64  # rows of one request per call
+    for b in range(B):
+        t0 = time.perf_counter()
+        sub_table = wl.page_table[b:b + 1]
+        oracle.kv_pack_ref(wl.rows_bits[b:b + 1, :per], sub_table, np.array([per], dtype=np.int32), wl.kv_scale,
+                           cache, "fp8_e4m3")
+        t_total += time.perf_counter() - t0
+        rows += per
+        if t_total >= budget_s:
+            break
+    return rows / t_total, {"rows": rows, "seconds": t_total, "cores": len(os.sched_getaffinity(0))}
+
+
+def run_kv_pack(args):
+    """The cache write, timed like the decode: device events around the one
+    launch per step, inputs (302 MB of rows) larger than L2 and L2 flushed
+    between steps; e2e adds the H2D copy of the rows from pinned memory and
+    the D2H read of the status word."""
+    import torch
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.build import build_library
+
+    build_library()
+    mla.load_library()
+    wl = W.kv_pack_batch(seed=2000 + 7919 * rank if args.seed is None else args.seed + 7919 * rank)
+    B, n_new, _ = wl.rows_bits.shape
+    n_rows = B * n_new
+    rows = torch.from_numpy(wl.rows_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    cache = torch.zeros(wl.num_pages, 64, 576, dtype=torch.uint8, device=dev)
+    pt = torch.from_numpy(wl.page_table).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        mla.mla_kv_pack(rows, pt, sl, wl.kv_scale, cache, status, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_k = [a.elapsed_time(b) for a, b in ev]
+    ms, job_rows = reduce_over_ranks(float(np.mean(ms_k)), n_rows, dev)
+    value = job_rows / (ms * 1e-3)
+    st = int(status.item())
+
+    # end to end: the rows arrive from pinned host memory every step
+    h_rows = rows.cpu().pin_memory()
+    h_status = torch.empty(1, dtype=torch.int32).pin_memory()
+    h2d, d2h = h_rows.numel() * h_rows.element_size(), 4
+    e2e = []
+    for k in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        rows.copy_(h_rows, non_blocking=True)
+        step()
+        h_status.copy_(status, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e.append(a.elapsed_time(b))
+    e2e_ms, _ = reduce_over_ranks(float(np.mean(e2e)), n_rows, dev)
+
+    parity = None
+    if rank == 0 and not args.no_parity:  # sampled rows, bit-exact against the oracle
+        import oracle
+
+        rng = np.random.default_rng(1)
+        ok = True
+        for _ in range(64):
+            b, i = int(rng.integers(B)), int(rng.integers(n_new))
+            t = int(wl.seq_lens[b]) - n_new + i
+            got = cache[int(wl.page_table[b, t // 64]), t % 64].cpu().numpy()
+            ref = oracle.e4m3_encode(oracle.kv_pack.bf16_bits_to_f32(wl.rows_bits[b, i]) * (np.float32(1.0) / np.float32(wl.kv_scale)))
+            ok &= bool(np.array_equal(got, ref))
+        parity = {"rows_checked": 64, "bit_exact": ok}
+
+    hbm_peak, _, peak_src = measured_peaks()
+    nbytes = n_rows * (576 * 2 + 576)  # read a bf16 row, write its e4m3 codes
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, info = kv_pack_oracle_rate(wl, min(args.cpu_budget, 10.0))
+        cpu = {"value": rate, "unit": KV_PACK_UNIT, "cores": info["cores"], "kind": "oracle",
+               "sample": f"{info['rows']} rows of the kv_pack batch, numpy oracle, {info['seconds']:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": KV_PACK_METRIC, "value": value, "unit": KV_PACK_UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3", "data": "synthetic",
+            "config": {"workload": "kv_pack", **wl.describe(), "l2": "flushed between steps (512 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
+                         "kernel": "mla_kv_pack_kernel", "alg_bytes": nbytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": job_rows / (e2e_ms * 1e-3), "unit": KV_PACK_UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
+        }))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_reference_kv_pack(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    wl = W.kv_pack_batch(seed=2000 if args.seed is None else args.seed)
+    for _ in range(args.warmup):
+        kv_pack_oracle_rate(wl, 0.05)
+    rates, secs, info = [], [], None
+    for _ in range(args.steps):
+        r, info = kv_pack_oracle_rate(wl, args.ref_step_budget)
+        rates.append(r)
+        secs.append(info["seconds"])
+    value = float(np.mean(rates))
+    print(json.dumps({
+        "impl": "reference", "metric": KV_PACK_METRIC, "value": value, "unit": KV_PACK_UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "kv_pack", **wl.describe()},
+        "cpu_baseline": {"value": value, "unit": KV_PACK_UNIT, "cores": info["cores"], "kind": "oracle",
+                         "sample": f"{info['rows']} rows per step, numpy oracle"},
+        "e2e": {"value": value, "unit": KV_PACK_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,9 +598,12 @@ def main():
     ap.add_argument("--ref-step-budget", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--op", choices=["decode", "kv_pack"], default="decode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op == "kv_pack":
+        return run_reference_kv_pack(args) if args.impl == "reference" else run_kv_pack(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

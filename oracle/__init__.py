@@ -9,7 +9,8 @@ Parity status: every public function is pinned by ``tests/test_oracle_pins.py``
 against an independent check (non-absorbed attention, closed forms, the
 split/merge identity, brute force, and torch's own float8 decoder).
 """
-from .e4m3 import e4m3_decode_table, e4m3_to_f64
+from .e4m3 import e4m3_decode_table, e4m3_encode, e4m3_to_f64
+from .kv_pack import kv_pack_ref
 from .mla_oracle import (
     attend,
     bf16_bits_to_f64,
@@ -24,10 +25,12 @@ from .mla_oracle import (
 __all__ = [
     "attend",
     "e4m3_decode_table",
+    "e4m3_encode",
     "e4m3_to_f64",
     "bf16_bits_to_f64",
     "decode_cache_rows",
     "gather_rows",
+    "kv_pack_ref",
     "lse_merge",
     "mla_decode_ref",
     "mla_decode_ref_pieces",

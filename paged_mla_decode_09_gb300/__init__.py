@@ -1,4 +1,5 @@
-"""Paged MLA decode for GB300: Python binding of the C ABI in include/mla_decode.h.
+"""Paged MLA decode for GB300: Python binding of the C ABI in include/mla_decode.h
+and include/mla_kv_pack.h.
 
 The functions here only marshal arguments (torch tensors -> device
 pointers, shapes -> ``mla_dims``); every step of the decode runs in the
@@ -31,6 +32,7 @@ ENTRY_POINTS = (
     "mla_status_string",
     "mla_decode_launch_shape",
     "mla_decode_noalloc",
+    "mla_kv_pack",
 )
 
 
@@ -46,6 +48,17 @@ class MlaDims(ctypes.Structure):
         ("num_heads", ctypes.c_int32),
         ("q_len", ctypes.c_int32),
         ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("max_pages_per_req", ctypes.c_int32),
+        ("page_table_stride", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+    ]
+
+
+class MlaKvPackDims(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("num_new", ctypes.c_int32),
         ("num_pages", ctypes.c_int32),
         ("max_pages_per_req", ctypes.c_int32),
         ("page_table_stride", ctypes.c_int32),
@@ -91,6 +104,8 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.mla_decode_launch_shape.restype = ctypes.c_int
     lib.mla_decode_noalloc.argtypes = [D, P, P, P, P, P, I32, ctypes.c_float, ctypes.c_float, P, P, P, P]
     lib.mla_decode_noalloc.restype = ctypes.c_int
+    lib.mla_kv_pack.argtypes = [ctypes.POINTER(MlaKvPackDims), P, P, P, ctypes.c_float, P, P, P]
+    lib.mla_kv_pack.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -222,6 +237,26 @@ def mla_selftest_wait_timeout(workspace, timeout_us: int, stream=None) -> None:
     rc = load_library().mla_selftest_wait_timeout(_ptr(workspace), int(timeout_us), _stream_handle(stream))
     if rc != MLA_OK:
         raise MlaError(rc, "mla_selftest_wait_timeout")
+
+
+def mla_kv_pack(rows, page_table, seq_lens, kv_scale, kv_cache, status, stream=None) -> None:
+    """Enqueue the cache write of a step's new rows (see include/mla_kv_pack.h).
+
+    rows: bf16 [B, num_new, 576]; kv_cache: bf16 or uint8 (e4m3 codes)
+    [num_pages, 64, 576]; status: int32 [1] on the device (flags OR-ed in).
+    Raises MlaError on a host-side error.
+    """
+    _check_cuda(rows, page_table, seq_lens, kv_cache, status)
+    B, N, width = rows.shape
+    if width != 576 or not rows.is_contiguous():
+        raise ValueError("rows must be a contiguous [B, num_new, 576] tensor")
+    dims = MlaKvPackDims(batch=B, num_new=N, num_pages=int(kv_cache.shape[0]),
+                         max_pages_per_req=int(page_table.shape[1]), page_table_stride=int(page_table.stride(0)),
+                         kv_dtype=kv_dtype_code(kv_cache))
+    rc = load_library().mla_kv_pack(ctypes.byref(dims), _ptr(rows), _ptr(page_table), _ptr(seq_lens),
+                                    float(kv_scale), _ptr(kv_cache), _ptr(status), _stream_handle(stream))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_kv_pack")
 
 
 @dataclass

@@ -20,6 +20,12 @@ fp8        256   128   2   U{4096..16384}; E4M3 cache, one fp32 scale
 verify4    64    64    4   8192 each: kimi's shape verifying 3 draft tokens
 =========  ====  ====  ==  =================================================
 
+The cache write before a step (quantise-and-scatter of the new rows) is
+measured on its own batch, ``kv_pack_batch()``: 64 requests whose 4096-token
+prompts are all new (a Kimi-shaped prefill), N(0,1) bf16 rows written into
+an e4m3 cache of 4096 pages through a seeded page permutation, kv_scale =
+max|x| / 448 over the rows.
+
 Recipe (all integers drawn from one ``numpy.random.Generator(PCG64(seed))``
 in this order: sequence lengths, page permutation, q_nope, q_pe):
 
@@ -252,6 +258,34 @@ def custom(
 def default_seed(name: str) -> int:
     """Seed of a named batch: 1000 + its index in CONFIG_NAMES."""
     return 1000 + CONFIG_NAMES.index(name)
+
+
+@dataclass
+class KvPackBatch:
+    rows_bits: np.ndarray   # uint16 [B, num_new, 576]: bf16 bits of the new rows
+    page_table: np.ndarray  # int32 [B, pages per request]
+    seq_lens: np.ndarray    # int32 [B]; the new tokens are the last num_new positions
+    num_pages: int
+    kv_scale: float
+    seed: int
+
+    def describe(self) -> dict:
+        B, n_new, _ = self.rows_bits.shape
+        return {"batch": int(B), "num_new": int(n_new), "rows": int(B * n_new), "num_pages": int(self.num_pages),
+                "kv_dtype": "fp8_e4m3", "seed": self.seed}
+
+
+def kv_pack_batch(seed: int = 2000, batch: int = 64, num_new: int = 4096) -> KvPackBatch:
+    """The cache-write batch (module docstring): all of each prompt is new."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    pages_per_req = (num_new + PAGE_SIZE - 1) // PAGE_SIZE
+    pool = batch * pages_per_req
+    seq_lens = np.full(batch, num_new, dtype=np.int32)
+    perm = rng.permutation(pool).astype(np.int32)
+    table, _ = _tables_private(seq_lens, perm)
+    vals = _normal_pages(seed + 7919, batch * num_new // PAGE_SIZE).reshape(batch, num_new, D_ROW)
+    kv_scale = float(np.abs(vals).max()) / 448.0
+    return KvPackBatch(f32_to_bf16_bits(vals), table, seq_lens, pool, kv_scale, seed)
 
 
 def make_config(name: str, seed: int | None = None, sentinel: str = "nan") -> Workload:

@@ -125,3 +125,36 @@ def test_binding_refuses_cpu_tensors(lib):
     t = torch.zeros(2, 1, 16, 512, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mla.mla_decode(t, t, t, t, t, 1, 1.0, 1.0, t, t, t)
+
+
+def _pack_dims(**kw):
+    d = dict(batch=2, num_new=2, num_pages=16, max_pages_per_req=5, page_table_stride=5, kv_dtype=1)
+    d.update(kw)
+    return mla.MlaKvPackDims(**d)
+
+
+@pytest.mark.parametrize("bad", [dict(batch=0), dict(num_new=0), dict(num_pages=0), dict(max_pages_per_req=0),
+                                 dict(page_table_stride=4)])
+def test_kv_pack_invalid_dims_rejected_without_device(lib, bad):
+    d = _pack_dims(**bad)
+    assert lib.mla_kv_pack(ctypes.byref(d), P, P, P, 1.0, P, P, None) == -1
+
+
+def test_kv_pack_checks_type_scale_and_pointers(lib):
+    assert lib.mla_kv_pack(ctypes.byref(_pack_dims(kv_dtype=5)), P, P, P, 1.0, P, P, None) == -2
+    for s in (0.0, -1.0, float("nan"), float("inf")):
+        assert lib.mla_kv_pack(ctypes.byref(_pack_dims()), P, P, P, s, P, P, None) == -1
+    # a bf16 cache ignores kv_scale: only the pointer checks remain, and a
+    # misaligned row buffer is refused before the device is touched
+    M = ctypes.c_void_p(264)
+    assert lib.mla_kv_pack(ctypes.byref(_pack_dims(kv_dtype=0)), M, P, P, 0.0, P, P, None) == -3
+    assert lib.mla_kv_pack(ctypes.byref(_pack_dims()), P, P, P, 1.0, M, P, None) == -3
+    assert lib.mla_kv_pack(ctypes.byref(_pack_dims()), P, P, P, 1.0, P, None, None) == -1
+    assert lib.mla_kv_pack(None, P, P, P, 1.0, P, P, None) == -1
+
+
+def test_kv_pack_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    rows = torch.zeros(2, 1, 576, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mla.mla_kv_pack(rows, rows, rows, 1.0, rows, rows)

@@ -7,7 +7,10 @@
 * the split-KV pieces merged by log-sum-exp equal the unsplit result;
 * a pure-Python brute force with its own gather, math.fsum and a softmax
   without max subtraction;
-* torch's float8_e4m3fn decoder for every E4M3 code;
+* torch's float8_e4m3fn decoder for every E4M3 code, and its float8
+  conversion (round to nearest-even) for the encoder on in-range values;
+* the encoder's round trips, ties and saturation points derived by hand;
+* the cache write's scatter against positions computed independently;
 * causal masking of two draft positions against single-position calls;
 * page relabelling, prefix copies and tail sentinels leave the result alone.
 """
@@ -44,6 +47,89 @@ def test_e4m3_extremes():
     assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
     assert np.sum(np.isnan(t)) == 2
     assert t[0x80] == 0.0 and math.copysign(1.0, t[0x80]) == -1.0
+
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    t = oracle.e4m3_decode_table()
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(t[codes]), codes)
+
+
+def test_e4m3_encode_ties_go_to_the_even_code():
+    t = oracle.e4m3_decode_table()
+    # between consecutive positive values c and c + 1 the midpoint goes to
+    # whichever of the two has mantissa bit 0 clear; a hair off it goes to
+    # the nearer one
+    for c in range(0, 0x7E):
+        mid = (t[c] + t[c + 1]) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode([mid])[0] == even, c
+        assert oracle.e4m3_encode([mid - (t[c + 1] - t[c]) * 1e-3])[0] == c
+        assert oracle.e4m3_encode([mid + (t[c + 1] - t[c]) * 1e-3])[0] == c + 1
+        assert oracle.e4m3_encode([-mid])[0] == (even | 0x80)
+
+
+def test_e4m3_encode_saturation_zero_and_nan():
+    enc = oracle.e4m3_encode
+    assert list(enc([448.0, 449.0, 464.0, 480.0, 1e30, np.inf])) == [0x7E] * 6
+    assert list(enc([-448.0, -1e30, -np.inf])) == [0xFE] * 3
+    assert list(enc([2.0**-10, 2.0**-10 * 1.01, 2.0**-9 * 1.5, 2.0**-9 * 1.49])) == [0x00, 0x01, 0x02, 0x01]
+    assert list(enc([0.0, -0.0, -(2.0**-12)])) == [0x00, 0x80, 0x80]
+    assert enc([np.nan])[0] & 0x7F == 0x7F
+
+
+def test_e4m3_encode_matches_torch_rounding_in_range():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(5000) * 1e-2,
+                        rng.uniform(-448, 448, 5000)]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+
+
+def test_kv_pack_writes_exactly_the_new_positions():
+    rng = np.random.default_rng(9)
+    B, n_new, pages = 3, 3, 12
+    seq_lens = np.array([3, 66, 130], dtype=np.int32)
+    table = np.full((B, 4), -1, dtype=np.int32)
+    perm = rng.permutation(pages)
+    table[0, :1], table[1, :2], table[2, :3] = perm[:1], perm[1:3], perm[3:6]
+    rows = W.f32_to_bf16_bits(rng.standard_normal((B, n_new, 576)).astype(np.float32) * 30)
+    for kv_dtype, scale in (("bf16", 1.0), ("fp8_e4m3", 0.05)):
+        dt = np.uint16 if kv_dtype == "bf16" else np.uint8
+        cache = rng.integers(0, 200, size=(pages, 64, 576)).astype(dt)
+        out, status = oracle.kv_pack_ref(rows, table, seq_lens, scale, cache, kv_dtype)
+        assert status == 0
+        written = set()
+        for b in range(B):
+            for i in range(n_new):
+                t = int(seq_lens[b]) - n_new + i  # positions L-3, L-2, L-1
+                page, slot = int(table[b, t // 64]), t % 64
+                written.add((page, slot))
+                vals = (rows[b, i].astype(np.uint32) << 16).view(np.float32)
+                if kv_dtype == "bf16":
+                    assert np.array_equal(out[page, slot], rows[b, i])
+                else:  # decodes to the nearest e4m3 value of x / scale
+                    dec = oracle.e4m3_to_f64(out[page, slot])
+                    grid = oracle.e4m3_decode_table()[:0x7F]
+                    target = np.clip(np.abs(vals.astype(np.float64) / scale), 0, 448)
+                    best = np.min(np.abs(grid[None, :] - target[:, None]), axis=1)
+                    assert np.allclose(np.abs(np.abs(dec) - target), best, rtol=0, atol=1e-6 * (1 + target))
+        mask = np.ones((pages, 64), dtype=bool)
+        for page, slot in written:
+            mask[page, slot] = False
+        assert np.array_equal(out[mask], cache[mask])  # nothing else touched
+        assert len(written) == B * n_new
+
+
+def test_kv_pack_flags_bad_rows_and_skips_them():
+    table = np.array([[0, 99], [1, -1]], dtype=np.int32)
+    rows = np.zeros((2, 2, 576), dtype=np.uint16)
+    cache = np.zeros((4, 64, 576), dtype=np.uint8)
+    out, status = oracle.kv_pack_ref(rows, table, np.array([66, 1], dtype=np.int32), 1.0, cache, "fp8_e4m3")
+    assert status == 3  # page 99 is outside the pool; length 1 < 2 new tokens
+    out, status = oracle.kv_pack_ref(rows, table, np.array([64, 200], dtype=np.int32), 1.0, cache, "fp8_e4m3")
+    assert status == 2  # 200 > 2 pages * 64
 
 
 def test_bf16_decode_patterns():
