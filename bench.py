@@ -9,6 +9,7 @@ each, 64-token pages, bf16 latent cache).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
     python bench.py --impl reference ...   # the CPU float64 oracle instead
     python bench.py --op kv_pack ...       # the cache write before a step
+    python bench.py --op sparse ...        # top-k decode on the dsa batch
 
 ``--op kv_pack``: one step = one quantise-and-scatter of a Kimi-shaped
 prefill (64 requests x 4096 new tokens) into an e4m3 cache; metric rows/s.
@@ -561,6 +562,181 @@ def run_kv_pack(args):
     return 0
 
 
+SPARSE_METRIC = "MLA top-k decode picked-KV-tokens/s"
+
+
+def sparse_oracle_rate(wl, idx, budget_s: float):
+    """picked-KV-tokens/s of the float64 oracle on a bounded sample of requests."""
+    import oracle
+
+    done, t_total, reqs = 0, 0.0, 0
+    for b in range(wl.batch):
+        t0 = time.perf_counter()
+        oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len, idx,
+                                     wl.scale, wl.kv_scale, wl.kv_dtype, requests=[b])
+        t_total += time.perf_counter() - t0
+        done += int((idx[b] >= 0).sum())
+        reqs += 1
+        if t_total >= budget_s:
+            break
+    return done / t_total, {"requests": reqs, "picked": done, "seconds": t_total,
+                            "cores": len(os.sched_getaffinity(0))}
+
+
+def run_sparse(args):
+    """Top-k decode of the dsa batch: one step = gather of the picked rows +
+    the paged decode over them, timed with device events around the call."""
+    import torch
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.build import build_library
+    from paged_mla_decode_09_gb300.device_inputs import to_device
+
+    build_library()
+    mla.load_library()
+    wl = W.make_config("dsa", seed=rank_seed(args.seed, "dsa", rank))
+    topk = int(wl.meta["topk"])
+    idx = W.topk_indices(wl, topk, seed=rank_seed(args.seed, "dsa", rank) + 1)
+    db = to_device(wl, dev)
+    ix = torch.from_numpy(idx).to(dev)
+    dims = mla.make_dims(db.q_nope, db.kv_cache, db.page_table)
+    ws = torch.zeros(mla.mla_decode_sparse_workspace_size(dims, topk, dev.index), dtype=torch.uint8, device=dev)
+    B, Q, H, _ = db.q_nope.shape
+    out = torch.empty(B, Q, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Q, H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        mla.mla_decode_sparse(db.q_nope, db.q_pe, db.kv_cache, db.page_table, db.seq_lens, ix, db.scale,
+                              db.kv_scale, out, lse, ws, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = mla.mla_decode_sparse_query_status(db.q_nope, db.kv_cache, db.page_table, topk, ws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    picked = int((idx >= 0).sum())
+    ms, job_picked = reduce_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), picked, dev)
+    value = job_picked / (ms * 1e-3)
+
+    # end to end: queries and picks arrive from pinned memory, out and lse go back
+    h_in = [t.cpu().pin_memory() for t in (db.q_nope, db.q_pe, ix)]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    e2e = []
+    for k in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for d_t, h_t in zip((db.q_nope, db.q_pe, ix), h_in):
+            d_t.copy_(h_t, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e.append(a.elapsed_time(b))
+    e2e_ms, _ = reduce_over_ranks(float(np.mean(e2e)), picked, dev)
+
+    parity = None
+    if rank == 0 and not args.no_parity:
+        import oracle
+
+        reqs = [0, B - 1]
+        ro, rl, _ = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens,
+                                                 wl.q_len, idx, wl.scale, requests=reqs)
+        go = h_out.float().numpy().astype(np.float64)
+        gl = h_lse.numpy().astype(np.float64)
+        eo, el = np.abs(go[reqs] - ro[reqs]), np.abs(gl[reqs] - rl[reqs])
+        parity = {"requests": reqs, "max_abs_out": float(eo.max()), "max_abs_lse": float(el.max()),
+                  "within_tol": bool(np.all(eo <= 1e-2 + 1e-2 * np.abs(ro[reqs])) and
+                                     np.all(el <= 1e-2 + 1e-2 * np.abs(rl[reqs])))}
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    nbytes = picked * 1152 + sum(t.numel() * t.element_size() for t in (db.q_nope, db.q_pe, ix, out, lse))
+    flops = picked * H * FLOP_PER_ROW_TOKEN
+    t_b, t_f = nbytes / (hbm_peak * 1e9), flops / (bf16_peak * 1e12)
+    if t_b >= t_f:
+        roof = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": bf16_peak, "unit": "TFLOP/s"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "peak_source": peak_src,
+                 "kernel": "mla_topk_gather_kernel + decode (whole step)", "alg_bytes": nbytes, "alg_flops": flops})
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, info = sparse_oracle_rate(wl, idx, min(args.cpu_budget, 10.0))
+        cpu = {"value": rate, "unit": "picked-KV-tokens/s", "cores": info["cores"], "kind": "oracle",
+               "sample": f"{info['requests']} request(s) of the dsa batch, float64 oracle, {info['seconds']:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": SPARSE_METRIC, "value": value, "unit": "picked-KV-tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "dsa", **wl.describe(), "topk": topk,
+                       "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": job_picked / (e2e_ms * 1e-3), "unit": "picked-KV-tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            # gather, schedule, attention, combine
+            "gpu_launches": 4 * args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
+        }))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_reference_sparse(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    wl = W.make_config("dsa", seed=args.seed)
+    idx = W.topk_indices(wl, int(wl.meta["topk"]), seed=(W.default_seed("dsa") if args.seed is None else args.seed) + 1)
+    for _ in range(args.warmup):
+        sparse_oracle_rate(wl, idx, 0.05)
+    rates, secs, info = [], [], None
+    for _ in range(args.steps):
+        r, info = sparse_oracle_rate(wl, idx, args.ref_step_budget)
+        rates.append(r)
+        secs.append(info["seconds"])
+    value = float(np.mean(rates))
+    print(json.dumps({
+        "impl": "reference", "metric": SPARSE_METRIC, "value": value, "unit": "picked-KV-tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "dsa", **wl.describe(), "topk": int(wl.meta["topk"])},
+        "cpu_baseline": {"value": value, "unit": "picked-KV-tokens/s", "cores": info["cores"], "kind": "oracle",
+                         "sample": f"{info['requests']} request(s) per step, float64 oracle"},
+        "e2e": {"value": value, "unit": "picked-KV-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
 def run_reference_kv_pack(args):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -598,12 +774,14 @@ def main():
     ap.add_argument("--ref-step-budget", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
-    ap.add_argument("--op", choices=["decode", "kv_pack"], default="decode")
+    ap.add_argument("--op", choices=["decode", "kv_pack", "sparse"], default="decode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.op == "kv_pack":
         return run_reference_kv_pack(args) if args.impl == "reference" else run_kv_pack(args)
+    if args.op == "sparse":
+        return run_reference_sparse(args) if args.impl == "reference" else run_sparse(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

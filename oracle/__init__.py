@@ -11,6 +11,7 @@ split/merge identity, brute force, and torch's own float8 decoder).
 """
 from .e4m3 import e4m3_decode_table, e4m3_encode, e4m3_to_f64
 from .kv_pack import kv_pack_ref
+from .sparse import mla_decode_sparse_ref
 from .mla_oracle import (
     attend,
     bf16_bits_to_f64,
@@ -34,5 +35,6 @@ __all__ = [
     "lse_merge",
     "mla_decode_ref",
     "mla_decode_ref_pieces",
+    "mla_decode_sparse_ref",
     "visible_keys",
 ]

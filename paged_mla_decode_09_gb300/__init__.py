@@ -1,5 +1,5 @@
-"""Paged MLA decode for GB300: Python binding of the C ABI in include/mla_decode.h
-and include/mla_kv_pack.h.
+"""Paged MLA decode for GB300: Python binding of the C ABI in include/mla_decode.h,
+include/mla_kv_pack.h and include/mla_sparse.h.
 
 The functions here only marshal arguments (torch tensors -> device
 pointers, shapes -> ``mla_dims``); every step of the decode runs in the
@@ -21,6 +21,7 @@ MLA_DEV_BAD_PAGE_ID = 1
 MLA_DEV_BAD_SEQ_LEN = 2
 MLA_DEV_TIMEOUT = 4
 MLA_DEV_INTERNAL = 8
+MLA_DEV_BAD_INDEX = 16
 
 ENTRY_POINTS = (
     "mla_decode_workspace_size",
@@ -33,6 +34,9 @@ ENTRY_POINTS = (
     "mla_decode_launch_shape",
     "mla_decode_noalloc",
     "mla_kv_pack",
+    "mla_decode_sparse_workspace_size",
+    "mla_decode_sparse",
+    "mla_decode_sparse_query_status",
 )
 
 
@@ -106,6 +110,12 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.mla_decode_noalloc.restype = ctypes.c_int
     lib.mla_kv_pack.argtypes = [ctypes.POINTER(MlaKvPackDims), P, P, P, ctypes.c_float, P, P, P]
     lib.mla_kv_pack.restype = ctypes.c_int
+    lib.mla_decode_sparse_workspace_size.argtypes = [D, I32, ctypes.c_int]
+    lib.mla_decode_sparse_workspace_size.restype = SZ
+    lib.mla_decode_sparse.argtypes = [D, P, P, P, P, P, P, I32, I32, ctypes.c_float, ctypes.c_float, P, P, P, SZ, P]
+    lib.mla_decode_sparse.restype = ctypes.c_int
+    lib.mla_decode_sparse_query_status.argtypes = [D, I32, P, P, ctypes.POINTER(I32)]
+    lib.mla_decode_sparse_query_status.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -257,6 +267,43 @@ def mla_kv_pack(rows, page_table, seq_lens, kv_scale, kv_cache, status, stream=N
                                     float(kv_scale), _ptr(kv_cache), _ptr(status), _stream_handle(stream))
     if rc != MLA_OK:
         raise MlaError(rc, "mla_kv_pack")
+
+
+def mla_decode_sparse_workspace_size(dims: MlaDims, topk: int, device: int | None = None) -> int:
+    import torch
+
+    dev = torch.cuda.current_device() if device is None else device
+    n = load_library().mla_decode_sparse_workspace_size(ctypes.byref(dims), int(topk), dev)
+    if n == 0:
+        raise MlaError(-1, "mla_decode_sparse_workspace_size")
+    return int(n)
+
+
+def mla_decode_sparse(q_nope, q_pe, kv_cache, page_table, seq_lens, indices, scale, kv_scale, out, lse, workspace,
+                      stream=None) -> None:
+    """Enqueue a top-k decode (see include/mla_sparse.h); indices: int32
+    [B, q_len, topk] token positions, -1 = unused."""
+    _check_cuda(q_nope, q_pe, kv_cache, page_table, seq_lens, indices, out, lse, workspace)
+    B, Q, topk = indices.shape
+    if (B, Q) != tuple(q_nope.shape[:2]) or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous [B, q_len, topk] tensor")
+    dims = make_dims(q_nope, kv_cache, page_table)
+    rc = load_library().mla_decode_sparse(
+        ctypes.byref(dims), _ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(page_table), _ptr(seq_lens),
+        _ptr(indices), int(topk), int(Q), float(scale), float(kv_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_decode_sparse")
+
+
+def mla_decode_sparse_query_status(q_nope, kv_cache, page_table, topk: int, workspace, stream=None) -> int:
+    dims = make_dims(q_nope, kv_cache, page_table)
+    st = ctypes.c_int32(0)
+    rc = load_library().mla_decode_sparse_query_status(ctypes.byref(dims), int(topk), _ptr(workspace),
+                                                        _stream_handle(stream), ctypes.byref(st))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_decode_sparse_query_status")
+    return st.value
 
 
 @dataclass

@@ -18,7 +18,13 @@ dsv3       128   128   1   floor(exp(U(ln 1024, ln 32768))); split-KV needed
 prefix     32    64    1   768 shared prefix pages + U{1024..4096} private
 fp8        256   128   2   U{4096..16384}; E4M3 cache, one fp32 scale
 verify4    64    64    4   8192 each: kimi's shape verifying 3 draft tokens
+dsa        64    128   1   16384 each; top-k decode over 2048 picked rows
 =========  ====  ====  ==  =================================================
+
+``dsa`` is a DeepSeek-V3.2-shaped batch for the top-k (sparse) decode: its
+picked positions come from ``topk_indices``: for every (request, draft
+position) a seeded random subset of the visible positions of size
+min(topk, visible), in random order, padded with -1.
 
 The cache write before a step (quantise-and-scatter of the new rows) is
 measured on its own batch, ``kv_pack_batch()``: 64 requests whose 4096-token
@@ -60,7 +66,7 @@ _CHUNK_PAGES = 256
 BF16_NAN = np.uint16(0x7FC0)
 E4M3_NAN = np.uint8(0x7F)
 
-CONFIG_NAMES = ("tiny", "kimi", "dsv3", "prefix", "fp8", "verify4")
+CONFIG_NAMES = ("tiny", "kimi", "dsv3", "prefix", "fp8", "verify4", "dsa")
 
 
 @dataclass
@@ -219,6 +225,20 @@ def build(
     )
 
 
+def topk_indices(wl: "Workload", topk: int, seed: int) -> np.ndarray:
+    """int32 [B, q_len, topk]: for each (request, draft position) a seeded
+    random subset of its visible positions (min(topk, visible) of them, in
+    random order), padded with -1."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.full((wl.batch, wl.q_len, topk), -1, dtype=np.int32)
+    for b in range(wl.batch):
+        for i in range(wl.q_len):
+            n = int(wl.seq_lens[b]) - wl.q_len + i + 1
+            k = min(topk, n)
+            out[b, i, :k] = rng.choice(n, size=k, replace=False)
+    return out
+
+
 def _tables_private(seq_lens, perm, extra_cols: int = 0):
     """Hand out permuted page ids request by request."""
     npg = [(int(L) + PAGE_SIZE - 1) // PAGE_SIZE for L in seq_lens]
@@ -340,6 +360,13 @@ def make_config(name: str, seed: int | None = None, sentinel: str = "nan") -> Wo
         perm = rng.permutation(pool).astype(np.int32)
         table, _ = _tables_private(seq_lens, perm)
         return build(name, H, 2, seq_lens, table, pool, rng, seed, "fp8_e4m3", sentinel=sentinel)
+    if name == "dsa":
+        B, H, L = 64, 128, 16384
+        seq_lens = np.full(B, L, dtype=np.int32)
+        pool = B * (L // PAGE_SIZE)
+        perm = rng.permutation(pool).astype(np.int32)
+        table, _ = _tables_private(seq_lens, perm)
+        return build(name, H, 1, seq_lens, table, pool, rng, seed, "bf16", sentinel=sentinel, meta={"topk": 2048})
     if name == "verify4":
         # speculative verification: the new token and 3 drafts per request,
         # causal among themselves; 4 * 64 = 256 query rows per request

@@ -427,3 +427,87 @@ def test_named_workload_shapes_small():
     used = set(wl.page_table[0, :2]) | set(wl.page_table[1, :5])
     assert len(used) == 7 and all(0 <= p < 16 for p in used)
     assert abs(wl.scale - 1 / math.sqrt(192)) < 1e-15
+
+
+# ------------------------------------------------------------ top-k decode
+def _sparse_case(kv_dtype="bf16", q_len=2):
+    wl = W.custom([130, 70, 300], num_heads=8, q_len=q_len, kv_dtype=kv_dtype, seed=61)
+    return wl
+
+
+def test_sparse_with_every_visible_position_is_the_dense_decode():
+    wl = _sparse_case()
+    idx = np.full((wl.batch, wl.q_len, 320), -1, dtype=np.int32)
+    for b in range(wl.batch):
+        for i in range(wl.q_len):
+            n = int(wl.seq_lens[b]) - wl.q_len + i + 1
+            idx[b, i, :n] = np.arange(n)
+    o, l, st = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len,
+                                            idx, wl.scale)
+    ro, rl = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len, wl.scale)
+    assert st == 0
+    assert np.allclose(o, ro, rtol=0, atol=1e-12) and np.allclose(l, rl, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_sparse_equals_dense_over_a_cache_of_the_picked_rows(kv_dtype):
+    """Copy the picked rows (in list order) into a fresh paged cache and run
+    the dense decode over it: same result (position i sees all its picks)."""
+    wl = _sparse_case(kv_dtype, q_len=1)
+    idx = W.topk_indices(wl, 90, seed=4)
+    o, l, st = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 1, idx,
+                                            wl.scale, wl.kv_scale, kv_dtype)
+    assert st == 0
+    for b in range(wl.batch):
+        picks = [int(t) for t in idx[b, 0] if t >= 0]
+        rows = np.stack([wl.kv_cache[wl.page_table[b, t // 64], t % 64] for t in picks])
+        npg = (len(picks) + 63) // 64
+        cache = np.zeros((npg, 64, 576), dtype=wl.kv_cache.dtype)
+        cache.reshape(-1, 576)[:len(picks)] = rows
+        table = np.arange(npg, dtype=np.int32)[None, :]
+        ro, rl = mla_decode_ref(wl.q_nope[b:b + 1], wl.q_pe[b:b + 1], cache, table,
+                                np.array([len(picks)], dtype=np.int32), 1, wl.scale, wl.kv_scale, kv_dtype)
+        assert np.allclose(o[b], ro[0], rtol=0, atol=1e-12) and np.allclose(l[b], rl[0], rtol=0, atol=1e-12)
+
+
+def test_sparse_closed_forms_single_and_repeated_pick():
+    wl = _sparse_case(q_len=1)
+    t = 45
+    one = np.array([[[t, -1, -1]]] * wl.batch, dtype=np.int32)
+    two = np.array([[[t, t, -1]]] * wl.batch, dtype=np.int32)
+    o1, l1, s1 = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 1, one,
+                                              wl.scale)
+    o2, l2, s2 = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 1, two,
+                                              wl.scale)
+    assert s1 == s2 == 0
+    for b in range(wl.batch):
+        row = oracle.bf16_bits_to_f64(wl.kv_cache[wl.page_table[b, 0], t])[:512]
+        assert np.array_equal(o1[b, 0], np.broadcast_to(row, o1[b, 0].shape))  # one key: its latent row
+    assert np.allclose(o2, o1, rtol=0, atol=1e-15)
+    assert np.allclose(l2, l1 + math.log(2.0), rtol=0, atol=1e-12)  # twice the same key: lse + ln 2
+
+
+def test_sparse_pick_order_does_not_matter():
+    wl = _sparse_case()
+    idx = W.topk_indices(wl, 50, seed=8)
+    rev = idx[:, :, ::-1].copy()
+    a = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, idx, wl.scale)
+    b = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, rev, wl.scale)
+    assert np.allclose(a[0], b[0], rtol=0, atol=1e-12) and np.allclose(a[1], b[1], rtol=0, atol=1e-12)
+
+
+def test_sparse_bad_entries_are_flagged_and_skipped():
+    wl = _sparse_case(q_len=2)
+    idx = np.array([[[0, 5, 129, 128, -1], [0, 5, 129, -7, -1]]] * wl.batch, dtype=np.int32)
+    # request 0 has L=130: draft 0 sees 0..128, draft 1 sees 0..129
+    ok = np.array([[[0, 5, 128, -1, -1], [0, 5, 129, -1, -1]]] * wl.batch, dtype=np.int32)
+    a = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, idx, wl.scale,
+                                     requests=[0])
+    b = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, ok, wl.scale,
+                                     requests=[0])
+    assert a[2] == oracle.sparse.BAD_INDEX and b[2] == 0
+    assert np.allclose(a[0][0], b[0][0], rtol=0, atol=1e-15)
+    empty = np.full((wl.batch, 2, 3), -1, dtype=np.int32)
+    o, l, st = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, empty,
+                                            wl.scale, requests=[1])
+    assert st == oracle.sparse.BAD_INDEX and np.all(o[1] == 0) and np.all(l[1] == 0)
