@@ -123,13 +123,17 @@ def test_kv_pack_writes_exactly_the_new_positions():
 
 
 def test_kv_pack_flags_bad_rows_and_skips_them():
+    rng = np.random.default_rng(12)
     table = np.array([[0, 99], [1, -1]], dtype=np.int32)
-    rows = np.zeros((2, 2, 576), dtype=np.uint16)
-    cache = np.zeros((4, 64, 576), dtype=np.uint8)
+    rows = W.f32_to_bf16_bits(rng.standard_normal((2, 2, 576)).astype(np.float32))
+    cache = rng.integers(0, 120, size=(4, 64, 576)).astype(np.uint8)
     out, status = oracle.kv_pack_ref(rows, table, np.array([66, 1], dtype=np.int32), 1.0, cache, "fp8_e4m3")
     assert status == 3  # page 99 is outside the pool; length 1 < 2 new tokens
+    assert np.array_equal(out, cache)  # neither bad row was written anywhere
     out, status = oracle.kv_pack_ref(rows, table, np.array([64, 200], dtype=np.int32), 1.0, cache, "fp8_e4m3")
     assert status == 2  # 200 > 2 pages * 64
+    changed = np.argwhere(np.any(out != cache, axis=2))
+    assert {tuple(x) for x in changed} <= {(0, 62), (0, 63)}  # only request 0's two rows
 
 
 def test_bf16_decode_patterns():
