@@ -10,6 +10,7 @@ each, 64-token pages, bf16 latent cache).
     python bench.py --impl reference ...   # the CPU float64 oracle instead
     python bench.py --op kv_pack ...       # the cache write before a step
     python bench.py --op sparse ...        # top-k decode on the dsa batch
+    python bench.py --op cascade ...       # shared-prefix cascade on the prefix batch
 
 ``--op kv_pack``: one step = one quantise-and-scatter of a Kimi-shaped
 prefill (64 requests x 4096 new tokens) into an e4m3 cache; metric rows/s.
@@ -711,6 +712,130 @@ def run_sparse(args):
     return 0
 
 
+def run_cascade(args):
+    """The prefix batch through the cascade entry point (prefix pass, suffix
+    pass, merge), timed with device events around the call; same metric and
+    algorithmic work as the plain decode of that batch."""
+    import torch
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.build import build_library
+    from paged_mla_decode_09_gb300.device_inputs import out_to_f64, to_device
+
+    build_library()
+    mla.load_library()
+    wl = W.make_config("prefix", seed=rank_seed(args.seed, "prefix", rank))
+    npre = int(wl.meta["shared_prefix_pages"])
+    db = to_device(wl, dev)
+    dims = mla.make_dims(db.q_nope, db.kv_cache, db.page_table)
+    ws = torch.zeros(mla.mla_decode_cascade_workspace_size(dims, npre, dev.index), dtype=torch.uint8, device=dev)
+    B, Q, H, _ = db.q_nope.shape
+    out = torch.empty(B, Q, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Q, H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        mla.mla_decode_cascade(db.q_nope, db.q_pe, db.kv_cache, db.page_table, db.seq_lens, npre, db.scale,
+                               db.kv_scale, out, lse, ws, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = mla.mla_decode_cascade_query_status(db.q_nope, db.kv_cache, db.page_table, npre, ws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms, job_tokens = reduce_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), wl.kv_tokens, dev)
+    value = job_tokens / (ms * 1e-3)
+
+    h_in = [t.cpu().pin_memory() for t in (db.q_nope, db.q_pe, db.page_table, db.seq_lens)]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    e2e = []
+    for k in range(args.warmup + args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for d_t, h_t in zip((db.q_nope, db.q_pe, db.page_table, db.seq_lens), h_in):
+            d_t.copy_(h_t, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            e2e.append(a.elapsed_time(b))
+    e2e_ms, _ = reduce_over_ranks(float(np.mean(e2e)), wl.kv_tokens, dev)
+
+    parity = None
+    if rank == 0 and not args.no_parity:
+        import oracle
+
+        reqs = [0, B - 1]
+        ro, rl = oracle.mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len,
+                                       wl.scale, wl.kv_scale, wl.kv_dtype, requests=reqs)
+        go, gl = out_to_f64(h_out), h_lse.numpy().astype(np.float64)
+        eo, el = np.abs(go[reqs] - ro[reqs]), np.abs(gl[reqs] - rl[reqs])
+        parity = {"requests": reqs, "max_abs_out": float(eo.max()), "max_abs_lse": float(el.max()),
+                  "within_tol": bool(np.all(eo <= 1e-2 + 1e-2 * np.abs(ro[reqs])) and
+                                     np.all(el <= 1e-2 + 1e-2 * np.abs(rl[reqs])))}
+    nbytes, flops, _ = algorithmic_work(wl)
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    t_b, t_f = nbytes / (hbm_peak * 1e9), flops / (bf16_peak * 1e12)
+    if t_b >= t_f:
+        roof = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": bf16_peak, "unit": "TFLOP/s"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "peak_source": peak_src,
+                 "kernel": "cascade step (prep, prefix decode, suffix decode, merge)", "alg_bytes": nbytes,
+                 "alg_flops": flops})
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, info = cpu_oracle_rate(wl, min(args.cpu_budget, 10.0))
+        cpu = {"value": rate, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+               "sample": f"{info['requests']} request(s) of the prefix batch, float64 oracle, {info['seconds']:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC + " (cascade)", "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prefix", **wl.describe(), "shared_prefix_pages": npre,
+                       "l2": "flushed between steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": job_tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            # prep, prefix pass (schedule, attention, combine), status, suffix pass (3), status, merge
+            "gpu_launches": 10 * args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
+        }))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def run_reference_sparse(args):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -774,12 +899,17 @@ def main():
     ap.add_argument("--ref-step-budget", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
-    ap.add_argument("--op", choices=["decode", "kv_pack", "sparse"], default="decode")
+    ap.add_argument("--op", choices=["decode", "kv_pack", "sparse", "cascade"], default="decode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.op == "kv_pack":
         return run_reference_kv_pack(args) if args.impl == "reference" else run_kv_pack(args)
+    if args.op == "cascade":
+        if args.impl == "reference":  # the cascade computes the plain decode: same oracle arm
+            args.config = "prefix"
+            return run_reference(args)
+        return run_cascade(args)
     if args.op == "sparse":
         return run_reference_sparse(args) if args.impl == "reference" else run_sparse(args)
     if args.impl == "reference":

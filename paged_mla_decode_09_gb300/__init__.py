@@ -1,5 +1,5 @@
 """Paged MLA decode for GB300: Python binding of the C ABI in include/mla_decode.h,
-include/mla_kv_pack.h and include/mla_sparse.h.
+include/mla_kv_pack.h, include/mla_sparse.h and include/mla_cascade.h.
 
 The functions here only marshal arguments (torch tensors -> device
 pointers, shapes -> ``mla_dims``); every step of the decode runs in the
@@ -22,6 +22,7 @@ MLA_DEV_BAD_SEQ_LEN = 2
 MLA_DEV_TIMEOUT = 4
 MLA_DEV_INTERNAL = 8
 MLA_DEV_BAD_INDEX = 16
+MLA_DEV_BAD_PREFIX = 32
 
 ENTRY_POINTS = (
     "mla_decode_workspace_size",
@@ -37,6 +38,9 @@ ENTRY_POINTS = (
     "mla_decode_sparse_workspace_size",
     "mla_decode_sparse",
     "mla_decode_sparse_query_status",
+    "mla_decode_cascade_workspace_size",
+    "mla_decode_cascade",
+    "mla_decode_cascade_query_status",
 )
 
 
@@ -116,6 +120,12 @@ def load_library(path: str | None = None, build: bool = False) -> ctypes.CDLL:
     lib.mla_decode_sparse.restype = ctypes.c_int
     lib.mla_decode_sparse_query_status.argtypes = [D, I32, P, P, ctypes.POINTER(I32)]
     lib.mla_decode_sparse_query_status.restype = ctypes.c_int
+    lib.mla_decode_cascade_workspace_size.argtypes = [D, I32, ctypes.c_int]
+    lib.mla_decode_cascade_workspace_size.restype = SZ
+    lib.mla_decode_cascade.argtypes = [D, P, P, P, P, P, I32, I32, ctypes.c_float, ctypes.c_float, P, P, P, SZ, P]
+    lib.mla_decode_cascade.restype = ctypes.c_int
+    lib.mla_decode_cascade_query_status.argtypes = [D, I32, P, P, ctypes.POINTER(I32)]
+    lib.mla_decode_cascade_query_status.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -303,6 +313,39 @@ def mla_decode_sparse_query_status(q_nope, kv_cache, page_table, topk: int, work
                                                         _stream_handle(stream), ctypes.byref(st))
     if rc != MLA_OK:
         raise MlaError(rc, "mla_decode_sparse_query_status")
+    return st.value
+
+
+def mla_decode_cascade_workspace_size(dims: MlaDims, prefix_pages: int, device: int | None = None) -> int:
+    import torch
+
+    dev = torch.cuda.current_device() if device is None else device
+    n = load_library().mla_decode_cascade_workspace_size(ctypes.byref(dims), int(prefix_pages), dev)
+    if n == 0:
+        raise MlaError(-1, "mla_decode_cascade_workspace_size")
+    return int(n)
+
+
+def mla_decode_cascade(q_nope, q_pe, kv_cache, page_table, seq_lens, prefix_pages, scale, kv_scale, out, lse,
+                       workspace, stream=None) -> None:
+    """Enqueue a cascade decode over a shared prefix (see include/mla_cascade.h)."""
+    _check_cuda(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace)
+    dims = make_dims(q_nope, kv_cache, page_table)
+    rc = load_library().mla_decode_cascade(
+        ctypes.byref(dims), _ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(page_table), _ptr(seq_lens),
+        int(prefix_pages), int(q_nope.shape[1]), float(scale), float(kv_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_decode_cascade")
+
+
+def mla_decode_cascade_query_status(q_nope, kv_cache, page_table, prefix_pages: int, workspace, stream=None) -> int:
+    dims = make_dims(q_nope, kv_cache, page_table)
+    st = ctypes.c_int32(0)
+    rc = load_library().mla_decode_cascade_query_status(ctypes.byref(dims), int(prefix_pages), _ptr(workspace),
+                                                         _stream_handle(stream), ctypes.byref(st))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_decode_cascade_query_status")
     return st.value
 
 

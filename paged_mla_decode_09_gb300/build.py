@@ -2,9 +2,9 @@
 
 ``python -m paged_mla_decode_09_gb300.build`` compiles
 ``csrc/mla_decode.cu`` (the decode), ``csrc/mla_kv_pack.cu`` (the cache
-write) and ``csrc/mla_sparse.cu`` (the top-k decode) with nvcc into
-``libmla_decode.so`` next to this file.  Three translation units, one
-``-gencode``; a few seconds.
+write), ``csrc/mla_sparse.cu`` (the top-k decode) and ``csrc/mla_cascade.cu``
+(the shared-prefix cascade) with nvcc into ``libmla_decode.so`` next to this
+file.  Four translation units, one ``-gencode``; a few seconds.
 """
 from __future__ import annotations
 
@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libmla_decode.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = [os.path.join(CSRC, f) for f in ("mla_decode.cu", "mla_kv_pack.cu", "mla_sparse.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("mla_decode.cu", "mla_kv_pack.cu", "mla_sparse.cu", "mla_cascade.cu")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -380,7 +380,7 @@ def make_config(name: str, seed: int | None = None, sentinel: str = "nan") -> Wo
 
 
 def prefix_shaped(batch: int, num_heads: int, prefix_pages: int, suffix_range, seed: int,
-                  kv_dtype: str = "bf16") -> Workload:
+                  kv_dtype: str = "bf16", q_len: int = 1) -> Workload:
     """A smaller prefix-shared batch: every table starts with the same pages."""
     rng = np.random.Generator(np.random.PCG64(seed))
     suffix = rng.integers(suffix_range[0], suffix_range[1], size=batch, endpoint=True).astype(np.int32)
@@ -394,7 +394,7 @@ def prefix_shaped(batch: int, num_heads: int, prefix_pages: int, suffix_range, s
     for b in range(batch):
         table[b, prefix_pages : prefix_pages + spg[b]] = perm[pos : pos + spg[b]]
         pos += spg[b]
-    return build("prefix_small", num_heads, 1, seq_lens, table, pool, rng, seed, kv_dtype,
+    return build("prefix_small", num_heads, q_len, seq_lens, table, pool, rng, seed, kv_dtype,
                  meta={"shared_prefix_pages": prefix_pages})
 
 
