@@ -158,3 +158,28 @@ def test_kv_pack_binding_refuses_cpu_tensors(lib):
     rows = torch.zeros(2, 1, 576, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mla.mla_kv_pack(rows, rows, rows, 1.0, rows, rows)
+
+
+def test_sparse_and_cascade_sizes_reject_bad_arguments(lib):
+    d = _dims()
+    assert lib.mla_decode_sparse_workspace_size(ctypes.byref(d), 0, 0) == 0      # top-k < 1
+    assert lib.mla_decode_sparse_workspace_size(ctypes.byref(d), 70000, 0) == 0  # top-k too large
+    assert lib.mla_decode_cascade_workspace_size(ctypes.byref(d), 0, 0) == 0     # no prefix
+    assert lib.mla_decode_cascade_workspace_size(ctypes.byref(d), 5, 0) == 0     # prefix = whole table
+    assert lib.mla_decode_cascade_workspace_size(ctypes.byref(_dims(num_heads=129, q_len=2)), 2, 0) == 0
+
+
+def test_sparse_and_cascade_reject_before_the_device(lib):
+    d = _dims()
+    args = (P, P, P, P, P)
+    assert lib.mla_decode_sparse(ctypes.byref(d), *args, None, 8, 1, 1.0, 1.0, P, P, P, 1 << 30, None) == -1
+    assert lib.mla_decode_sparse(ctypes.byref(d), *args, P, 0, 1, 1.0, 1.0, P, P, P, 1 << 30, None) == -1
+    assert lib.mla_decode_sparse(ctypes.byref(d), *args, P, 8, 2, 1.0, 1.0, P, P, P, 1 << 30, None) == -1  # q_len
+    assert lib.mla_decode_sparse(ctypes.byref(_dims(page_size=32)), *args, P, 8, 1, 1.0, 1.0, P, P, P, 1 << 30,
+                                 None) == -2
+    M = ctypes.c_void_p(258)
+    assert lib.mla_decode_sparse(ctypes.byref(d), *args, M, 8, 1, 1.0, 1.0, P, P, P, 1 << 30, None) == -3
+    assert lib.mla_decode_cascade(ctypes.byref(d), *args, 2, 1, 1.0, 1.0, P, P, None, 1 << 30, None) == -1
+    assert lib.mla_decode_cascade(ctypes.byref(d), *args, 2, 3, 1.0, 1.0, P, P, P, 1 << 30, None) == -1  # q_len
+    W = ctypes.c_void_p(256 + 64)
+    assert lib.mla_decode_cascade(ctypes.byref(d), *args, 2, 1, 1.0, 1.0, P, P, W, 1 << 30, None) == -3
