@@ -1144,14 +1144,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid < kPage) {
             // token rows past the sequence end may hold anything (even NaN):
             // zero them so that P = 0 there cannot turn into 0 * NaN
+            // lane: 16-byte chunk lane % 8 of rows v0 + lane / 8, + 4, ... in
+            // every box (no division: this warp is on the path to PV)
             const int v0 = valid > 0 ? valid : 0;
-            const int nrows = kPage - v0;
-            for (int idx = lane; idx < C::kBoxesPartO * nrows * 8; idx += 32) {
-              const int chunk = idx & 7;
-              const int rowi = (idx >> 3) % nrows + v0;
-              const int box = (idx >> 3) / nrows;
-              *reinterpret_cast<uint4*>(slot + box * C::kBox + rowi * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-            }
+            const int chunk = lane & 7;
+            for (int rowi = v0 + (lane >> 3); rowi < kPage; rowi += 4)
+#pragma unroll
+              for (int box = 0; box < C::kBoxesPartO; ++box)
+                *reinterpret_cast<uint4*>(slot + box * C::kBox + rowi * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
             fence_proxy_async_cta();
             __syncwarp();
           }
