@@ -19,7 +19,7 @@ namespace {
 
 constexpr int kPageRows = 64;
 constexpr int kChunkEntries = 256;  // top-k entries per gather block
-constexpr int kRowsInFlight = 4;    // rows a warp copies per round (all loads first)
+constexpr int kRowsInFlight = 2;    // rows a warp copies per round (all loads first; 1-8 measured, 1-2 best)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
