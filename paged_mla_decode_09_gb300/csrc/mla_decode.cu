@@ -18,11 +18,12 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Workspace: [status words | page prefix sums | cluster slices | fp32
-// partial outputs | partial log-sum-exps].  Sized by B, the cluster count
-// and the number of row blocks only.
+// Workspace: [status words | page prefix sums | cluster slices | each
+// request's first and last cluster | fp32 partial outputs | partial
+// log-sum-exps | e4m3 query scales].  Sized by B, the cluster count and the
+// number of row blocks only.
 struct Layout {
-  size_t status, prefix, cinfo, o_part, lse_part, qscale, total;
+  size_t status, prefix, cinfo, rrange, o_part, lse_part, qscale, total;
 };
 
 Layout workspace_layout(int B, int C, int G) {
@@ -30,7 +31,8 @@ Layout workspace_layout(int B, int C, int G) {
   l.status = 0;
   l.prefix = 256;
   l.cinfo = l.prefix + align256(static_cast<size_t>(B + 1) * 4);
-  l.o_part = l.cinfo + align256(static_cast<size_t>(C) * 3 * 4);
+  l.rrange = l.cinfo + align256(static_cast<size_t>(C) * 3 * 4);
+  l.o_part = l.rrange + align256(static_cast<size_t>(B) * 2 * 4);
   l.lse_part = l.o_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * mla::kDL * 4);
   l.qscale = l.lse_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * 4);
   l.total = l.qscale + align256(static_cast<size_t>(B) * G * mla::kRows * 4);  // e4m3 query scales
@@ -237,6 +239,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.status = reinterpret_cast<int32_t*>(ws + lay.status);
   p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
   p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
+  p.rrange = reinterpret_cast<int32_t*>(ws + lay.rrange);
   p.qscale = reinterpret_cast<float*>(ws + lay.qscale);
   p.B = d->batch;
   p.H = d->num_heads;
@@ -497,6 +500,7 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   p.status = reinterpret_cast<int32_t*>(ws + lay.status);
   p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
   p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
+  p.rrange = reinterpret_cast<int32_t*>(ws + lay.rrange);
   p.qscale = reinterpret_cast<float*>(ws + lay.qscale);
   p.B = d->batch;
   p.H = d->num_heads;

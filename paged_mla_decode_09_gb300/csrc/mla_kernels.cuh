@@ -205,6 +205,7 @@ struct Params {
   int32_t* status;         // [4]: status bits, timeout diagnostics
   int32_t* prefix;         // [B+1] page prefix sums
   int32_t* cinfo;          // [C][3] = slice start, slice end, first request
+  int32_t* rrange;         // [B][2] = first and last cluster whose slice meets the request
   float* qscale;           // [B * R] e4m3 query scales (e4m3 cache only)
   int32_t B, H, Q, R, G, C;
   int32_t num_pages, max_pages, pt_stride;
@@ -238,9 +239,19 @@ __device__ __forceinline__ int clamp_len(int L, int max_pages) {
 // ---------------------------------------------------------------- K0
 // Page prefix sums over requests and each cluster's page slice
 // [T*c/C, T*(c+1)/C) with the request holding its first page.
+constexpr int kSchedSmemB = 4096;     // requests whose prefix sums the schedule keeps in shared memory
+constexpr int kSchedSmemC = 512;      // clusters whose slices it keeps there
+
 __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
+  // the searches below run on shared-memory copies (a binary search over
+  // global memory is a chain of dependent loads); larger batches read the
+  // global arrays
+  __shared__ int32_t sp[kSchedSmemB + 1];
+  __shared__ int32_t cs[kSchedSmemC], ce[kSchedSmemC];
+  const bool sp_ok = p.B <= kSchedSmemB;
+  const bool c_ok = p.C <= kSchedSmemC;
   const int tid = threadIdx.x;
   if (tid == 0) carry = 0;
   __syncthreads();
@@ -269,29 +280,36 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     }
     __syncthreads();
     const int incl = v + ((tid >> 5) ? warp_tot[(tid >> 5) - 1] : 0) + carry;
-    if (b < p.B) p.prefix[b + 1] = incl;
+    if (b < p.B) {
+      p.prefix[b + 1] = incl;
+      if (sp_ok) sp[b + 1] = incl;
+    }
     __syncthreads();
     if (tid == 1023) carry = incl;
     __syncthreads();
   }
-  if (tid == 0) p.prefix[0] = 0;
+  if (tid == 0) {
+    p.prefix[0] = 0;
+    sp[0] = 0;
+  }
   __syncthreads();
+  const int32_t* pre = sp_ok ? sp : p.prefix;
   // Cluster slices are cut in a weighted order: request b occupies
   // p.unit_cost start-up units and then its pages, so clusters whose
   // slice starts many pieces get fewer pages.  A weighted position maps to
   // the page at that point (start-up units map to the request's first page).
-  const int64_t T = p.prefix[p.B];
+  const int64_t T = pre[p.B];
   const int64_t W = T + static_cast<int64_t>(p.unit_cost) * p.B;
   auto page_at = [&](int64_t x) -> int {
     int lo = 0, hi = p.B - 1;  // last request b with prefix[b] + unit_cost * b <= x
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.prefix[mid] + static_cast<int64_t>(p.unit_cost) * mid <= x) lo = mid; else hi = mid - 1;
+      if (pre[mid] + static_cast<int64_t>(p.unit_cost) * mid <= x) lo = mid; else hi = mid - 1;
     }
-    const int64_t np = p.prefix[lo + 1] - p.prefix[lo];
-    int64_t off = x - p.prefix[lo] - static_cast<int64_t>(p.unit_cost) * lo - p.unit_cost;
+    const int64_t np = pre[lo + 1] - pre[lo];
+    int64_t off = x - pre[lo] - static_cast<int64_t>(p.unit_cost) * lo - p.unit_cost;
     off = off < 0 ? 0 : (off > np ? np : off);
-    return static_cast<int>(p.prefix[lo] + off);
+    return static_cast<int>(pre[lo] + off);
   };
   for (int c = tid; c < p.C; c += 1024) {
     const int s = page_at(W * c / p.C);
@@ -299,11 +317,37 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     int lo = 0, hi = p.B - 1;  // last request b with prefix[b] <= s
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.prefix[mid] <= s) lo = mid; else hi = mid - 1;
+      if (pre[mid] <= s) lo = mid; else hi = mid - 1;
     }
     p.cinfo[3 * c + 0] = s;
     p.cinfo[3 * c + 1] = e;
     p.cinfo[3 * c + 2] = lo;
+    if (c_ok) {
+      cs[c] = s;
+      ce[c] = e;
+    }
+  }
+  __syncthreads();
+  // per request, the clusters whose slice [s, e) meets its pages
+  // [prefix[b], prefix[b+1]): from the first with e > prefix[b] to the last
+  // with s < prefix[b+1] (both bounds are non-decreasing in the cluster
+  // index); the combine merges the pieces of requests with more than one
+  for (int b = tid; b < p.B; b += 1024) {
+    const int pb0 = pre[b], pb1 = pre[b + 1];
+    int lo = 0, hi = p.C - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((c_ok ? ce[mid] : p.cinfo[3 * mid + 1]) > pb0) hi = mid; else lo = mid + 1;
+    }
+    const int clo = lo;
+    lo = 0;
+    hi = p.C - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((c_ok ? cs[mid] : p.cinfo[3 * mid]) < pb1) lo = mid; else hi = mid - 1;
+    }
+    p.rrange[2 * b] = pb1 > pb0 ? clo : 0;
+    p.rrange[2 * b + 1] = pb1 > pb0 ? lo : 0;
   }
 }
 
@@ -1338,28 +1382,9 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
   const int r = blockIdx.z * 8 + warp;
   const int rr = g * kRows + r;
   if (rr >= p.R) return;
-  const int pb0 = p.prefix[b], pb1 = p.prefix[b + 1];
-  if (pb1 <= pb0) return;
-  // clusters whose slice [s, e) meets the request's pages [pb0, pb1): from
-  // the first with e > pb0 to the last with s < pb1 (both bounds are
-  // non-decreasing in the cluster index)
-  int clo = 0, chi = p.C - 1;
-  {
-    int lo = 0, hi = p.C - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (p.cinfo[3 * mid + 1] > pb0) hi = mid; else lo = mid + 1;
-    }
-    clo = lo;
-    lo = 0;
-    hi = p.C - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.cinfo[3 * mid] < pb1) lo = mid; else hi = mid - 1;
-    }
-    chi = lo;
-  }
-  if (clo >= chi) return;  // the whole request in one slice: written directly
+  // the clusters whose slice meets the request (from the schedule)
+  const int clo = p.rrange[2 * b], chi = p.rrange[2 * b + 1];
+  if (clo >= chi) return;  // the whole request in one slice (or none): written directly
   // slices strictly between clo and chi may be empty (fewer pages than
   // clusters): an empty slice holds no piece and is skipped
   float mx = -INFINITY;
