@@ -18,6 +18,23 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Launches a kernel with programmatic stream serialization: it may start
+// while the previous kernel in the stream is finishing and waits for it
+// (griddep_wait) before reading that kernel's output.
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Workspace: [status words | page prefix sums | cluster slices | each
 // request's first and last cluster | fp32 partial outputs | partial
 // log-sum-exps | e4m3 query scales].  Sized by B, the cluster count and the
@@ -264,8 +281,11 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
   if (f8) {  // per-row e4m3 query scales
-    mla::mla_qscale_kernel<<<static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8), 256, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_pdl(mla::mla_qscale_kernel, dim3(static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8)),
+                   dim3(256), stream, p) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
   }
   if (!mark(1)) return MLA_ERR_CUDA;
 
@@ -274,13 +294,15 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   cfg.blockDim = dim3(mla::kThreads, 1, 1);
   cfg.dynamicSmemBytes = f8 ? Cfg<true>::kSmem : Cfg<false>::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2 * G;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // prologue overlaps the schedule
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe, maps.qn,
                                           maps.qp)
                      : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe,
@@ -290,8 +312,10 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
     return MLA_ERR_CUDA;
   }
   if (!mark(2)) return MLA_ERR_CUDA;
-  mla::mla_combine_kernel<<<dim3(d->batch, G, mla::kRows / 8), 256, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_pdl(mla::mla_combine_kernel, dim3(d->batch, G, mla::kRows / 8), dim3(256), stream, p) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
   if (!mark(3)) return MLA_ERR_CUDA;
   return MLA_OK;
 }
@@ -523,21 +547,26 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
   if (f8) {
-    mla::mla_qscale_kernel<<<static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8), 256, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_pdl(mla::mla_qscale_kernel, dim3(static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8)),
+                   dim3(256), stream, p) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * G * C, 1, 1);
   cfg.blockDim = dim3(mla::kThreads, 1, 1);
   cfg.dynamicSmemBytes = f8 ? Cfg<true>::kSmem : Cfg<false>::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2 * G;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // prologue overlaps the schedule
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe, maps.qn,
                                           maps.qp)
                      : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe,
@@ -546,8 +575,10 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
     cudaGetLastError();
     return MLA_ERR_CUDA;
   }
-  mla::mla_combine_kernel<<<dim3(d->batch, G, mla::kRows / 8), 256, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_pdl(mla::mla_combine_kernel, dim3(d->batch, G, mla::kRows / 8), dim3(256), stream, p) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
   if (status_out &&
       cudaMemcpyAsync(status_out, p.status, 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
     return MLA_ERR_CUDA;

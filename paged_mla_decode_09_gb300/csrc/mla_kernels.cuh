@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   __shared__ int32_t cs[kSchedSmemC], ce[kSchedSmemC];
   const bool sp_ok = p.B <= kSchedSmemB;
   const bool c_ok = p.C <= kSchedSmemC;
+  griddep_launch_dependents();  // the next kernels wait for this one before reading its output
   const int tid = threadIdx.x;
   if (tid == 0) carry = 0;
   __syncthreads();
@@ -355,9 +356,16 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
 // e4m3 cache: per query row r of request b, the scale of its e4m3 split,
 // max |q| / 448 over the 576 values (1 for an all-zero row).  One warp per row.
 __global__ void __launch_bounds__(256) mla_qscale_kernel(Params p) {
+  // needs nothing from the schedule, so it may run beside it; it ends only
+  // after the schedule has (griddep_wait below), so the attention kernel's
+  // wait for this one covers both
+  griddep_launch_dependents();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= static_cast<int64_t>(p.B) * p.R) return;
+  if (row >= static_cast<int64_t>(p.B) * p.R) {
+    griddep_wait();
+    return;
+  }
   const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
   const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + row * kDR * 2);
   float amax = 0.f;
@@ -373,6 +381,7 @@ __global__ void __launch_bounds__(256) mla_qscale_kernel(Params p) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if (lane == 0) p.qscale[row] = amax > 0.f ? amax / 448.f : 1.f;
+  griddep_wait();
 }
 
 // One request's piece inside a cluster's slice.
@@ -783,6 +792,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // partner barriers initialised before any remote arrive
+  // everything above overlaps the end of the kernel before this one; the
+  // schedule (and the e4m3 query scales) are read only after it completed
+  griddep_wait();
+  griddep_launch_dependents();  // the combine may launch as clusters finish
   const uint32_t tmem = ctrl->tmem_base;
   volatile int* abort = &ctrl->abort;
 #ifdef MLA_TRACE
@@ -1377,6 +1390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // lse = log sum_s exp(lse_s), out = sum_s exp(lse_s - lse) * out_s.
 
 __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
+  griddep_wait();  // the attention kernel's partials (and the schedule) are complete
   const int b = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.z * 8 + warp;

@@ -217,6 +217,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
 // bytes on `bar`.  x is the innermost coordinate (elements).
 // Pulls `bytes` (a multiple of 16) of global memory at `gaddr` (16-byte
 // aligned) into L2 without a destination in shared memory.
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel in the stream ends;
+// griddep_wait() blocks until that kernel has completed and its writes are
+// visible (a no-op for an ordinary launch); griddep_launch_dependents() lets
+// the next such kernel start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gaddr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gaddr)), "r"(bytes)
                : "memory");
