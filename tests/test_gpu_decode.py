@@ -256,3 +256,40 @@ def test_workspace_size_ignores_lengths():
     na = mla.mla_decode_workspace_size(mla.make_dims(da.q_nope, da.kv_cache, da.page_table))
     nb = mla.mla_decode_workspace_size(mla.make_dims(dbb.q_nope, dbb.kv_cache, dbb.page_table))
     assert na == nb
+
+
+def test_two_streams_at_once_equal_sequential_runs():
+    """The library keeps no state between calls: two batches decoded at the
+    same time on two streams (own workspaces) give bit for bit what they give
+    one after the other."""
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.device_inputs import out_to_f64, to_device
+
+    wls = [W.custom([3000, 700, 64], num_heads=64, q_len=1, seed=31),
+           W.custom([1200, 4100], num_heads=128, q_len=2, kv_dtype="fp8_e4m3", seed=32)]
+    dbs = [to_device(wl, "cuda") for wl in wls]
+    bufs = [mla.alloc_buffers(db.q_nope, db.kv_cache, db.page_table) for db in dbs]
+
+    def launch(k, stream=None):
+        db, bf = dbs[k], bufs[k]
+        mla.mla_decode(db.q_nope, db.q_pe, db.kv_cache, db.page_table, db.seq_lens, db.q_len, db.scale,
+                       db.kv_scale, bf.out, bf.lse, bf.workspace, stream)
+
+    seq = []
+    for k in range(2):
+        launch(k)
+        torch.cuda.synchronize()
+        seq.append((out_to_f64(bufs[k].out), bufs[k].lse.cpu().numpy().copy()))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        for k in range(2):
+            bufs[k].out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        for k in range(2):
+            with torch.cuda.stream(streams[k]):
+                launch(k, streams[k])
+        torch.cuda.synchronize()
+        for k in range(2):
+            assert mla.mla_query_status(bufs[k].workspace) == 0
+            assert np.array_equal(out_to_f64(bufs[k].out), seq[k][0])
+            assert np.array_equal(bufs[k].lse.cpu().numpy(), seq[k][1])
