@@ -76,6 +76,18 @@ def test_many_requests_few_pages():
     compare(wl, out, lse, label="many-short")
 
 
+def test_batch_beyond_schedule_shared_copy():
+    """More requests (4200) than the schedule keeps prefix sums for in shared
+    memory (4096): its searches run on the global copy, and request indices
+    past 4096 reach the combine."""
+    rng = np.random.default_rng(31)
+    lens = rng.integers(1, 140, size=4200).tolist()
+    wl = W.custom(lens, num_heads=8, q_len=1, seed=32)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    compare(wl, out, lse, label="B=4200")
+
+
 def test_long_pipeline_many_pages_per_cluster():
     """Hundreds of pages per cluster: every pipeline barrier wraps many times
     and output rescales happen on many pages."""
