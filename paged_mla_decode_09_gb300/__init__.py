@@ -201,6 +201,75 @@ def _check_cuda(*tensors):
             raise ValueError("all tensors must be CUDA tensors (the decode runs only on the GPU)")
 
 
+def _check_layout(name, t, shape, dtypes):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {list(shape)}, got {list(t.shape)}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must be {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_cache_and_table(kv_cache, page_table, seq_lens, B):
+    import torch
+
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != 576 or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be a contiguous [num_pages, page_size, 576] tensor")
+    kv_dtype_code(kv_cache)  # raises for other element types
+    if (page_table.dtype != torch.int32 or page_table.dim() != 2 or page_table.shape[0] != B
+            or page_table.stride(1) != 1 or page_table.stride(0) < page_table.shape[1]):
+        raise ValueError("page_table must be an int32 [B, max_pages] tensor with unit column stride")
+    _check_layout("seq_lens", seq_lens, (B,), (torch.int32,))
+
+
+def _check_decode_tensors(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace):
+    """The shapes, element types and layouts the C ABI assumes.  It receives
+    bare pointers, so a tensor that does not match (a broadcast view, another
+    dtype, a transposed copy) would be read or written with the wrong extent.
+    One combined test on the fast path (it runs on every call); the detailed
+    checks below name what is wrong."""
+    import torch
+
+    bf16, i32 = torch.bfloat16, torch.int32
+    s = q_nope.shape
+    if len(s) == 4:
+        B, Q, H = s[0], s[1], s[2]
+        dev = q_nope.get_device()
+        if (s[3] == 512 and q_nope.dtype is bf16 and q_nope.is_contiguous()
+                and q_pe.dtype is bf16 and q_pe.shape == (B, Q, H, 64) and q_pe.is_contiguous()
+                and out.dtype is bf16 and out.shape == s and out.is_contiguous()
+                and lse.dtype is torch.float32 and lse.shape == (B, Q, H) and lse.is_contiguous()
+                and seq_lens.dtype is i32 and seq_lens.shape == (B,) and seq_lens.is_contiguous()
+                and page_table.dtype is i32 and page_table.dim() == 2 and page_table.shape[0] == B
+                and page_table.stride(1) == 1 and page_table.stride(0) >= page_table.shape[1]
+                and kv_cache.dim() == 3 and kv_cache.shape[2] == 576 and kv_cache.is_contiguous()
+                and kv_cache.dtype in (bf16, torch.uint8, torch.float8_e4m3fn) and workspace.is_contiguous()
+                and q_pe.get_device() == dev and out.get_device() == dev and lse.get_device() == dev
+                and seq_lens.get_device() == dev and page_table.get_device() == dev
+                and kv_cache.get_device() == dev and workspace.get_device() == dev):
+            return
+    _explain_decode_tensors(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace)
+    raise ValueError("decode tensors do not have the shapes, types and layouts the library expects")
+
+
+def _explain_decode_tensors(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace):
+    import torch
+
+    if q_nope.dim() != 4 or q_nope.shape[3] != 512:
+        raise ValueError(f"q_nope must be [B, q_len, H, 512], got {list(q_nope.shape)}")
+    B, Q, H, _ = q_nope.shape
+    _check_layout("q_nope", q_nope, (B, Q, H, 512), (torch.bfloat16,))
+    _check_layout("q_pe", q_pe, (B, Q, H, 64), (torch.bfloat16,))
+    _check_layout("out", out, (B, Q, H, 512), (torch.bfloat16,))
+    _check_layout("lse", lse, (B, Q, H), (torch.float32,))
+    _check_cache_and_table(kv_cache, page_table, seq_lens, B)
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    for t in (q_pe, kv_cache, page_table, seq_lens, out, lse, workspace):
+        if t.device != q_nope.device:
+            raise ValueError("all tensors must be on one device")
+
+
 def mla_decode(q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, workspace,
                stream=None, events=None) -> None:
     """Enqueue one decode step (see include/mla_decode.h).  Raises MlaError on a host-side error.
@@ -209,6 +278,9 @@ def mla_decode(q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_sc
     to time the schedule / attention / combine launches.
     """
     _check_cuda(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace)
+    _check_decode_tensors(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace)
+    if int(q_len) != q_nope.shape[1]:
+        raise ValueError(f"q_len {q_len} does not match q_nope's second dimension {q_nope.shape[1]}")
     dims = make_dims(q_nope, kv_cache, page_table)
     lib = load_library()
     args = [ctypes.byref(dims), _ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(page_table), _ptr(seq_lens),
@@ -259,6 +331,19 @@ def mla_selftest_wait_timeout(workspace, timeout_us: int, stream=None) -> None:
         raise MlaError(rc, "mla_selftest_wait_timeout")
 
 
+def _check_kv_pack_tensors(rows, page_table, seq_lens, kv_cache, status):
+    import torch
+
+    if rows.dim() != 3 or rows.shape[2] != 576 or not rows.is_contiguous() or rows.dtype != torch.bfloat16:
+        raise ValueError("rows must be a contiguous bf16 [B, num_new, 576] tensor")
+    _check_cache_and_table(kv_cache, page_table, seq_lens, rows.shape[0])
+    if status.dtype != torch.int32 or status.numel() < 1:
+        raise ValueError("status must be an int32 tensor of at least one element")
+    for t in (page_table, seq_lens, kv_cache, status):
+        if t.device != rows.device:
+            raise ValueError("all tensors must be on one device")
+
+
 def mla_kv_pack(rows, page_table, seq_lens, kv_scale, kv_cache, status, stream=None) -> None:
     """Enqueue the cache write of a step's new rows (see include/mla_kv_pack.h).
 
@@ -267,9 +352,8 @@ def mla_kv_pack(rows, page_table, seq_lens, kv_scale, kv_cache, status, stream=N
     Raises MlaError on a host-side error.
     """
     _check_cuda(rows, page_table, seq_lens, kv_cache, status)
-    B, N, width = rows.shape
-    if width != 576 or not rows.is_contiguous():
-        raise ValueError("rows must be a contiguous [B, num_new, 576] tensor")
+    _check_kv_pack_tensors(rows, page_table, seq_lens, kv_cache, status)
+    B, N, _ = rows.shape
     dims = MlaKvPackDims(batch=B, num_new=N, num_pages=int(kv_cache.shape[0]),
                          max_pages_per_req=int(page_table.shape[1]), page_table_stride=int(page_table.stride(0)),
                          kv_dtype=kv_dtype_code(kv_cache))
@@ -289,14 +373,22 @@ def mla_decode_sparse_workspace_size(dims: MlaDims, topk: int, device: int | Non
     return int(n)
 
 
+def _check_indices(indices, q_nope):
+    import torch
+
+    if (indices.dim() != 3 or tuple(indices.shape[:2]) != tuple(q_nope.shape[:2]) or not indices.is_contiguous()
+            or indices.dtype != torch.int32 or indices.device != q_nope.device):
+        raise ValueError("indices must be a contiguous int32 [B, q_len, topk] tensor")
+
+
 def mla_decode_sparse(q_nope, q_pe, kv_cache, page_table, seq_lens, indices, scale, kv_scale, out, lse, workspace,
                       stream=None) -> None:
     """Enqueue a top-k decode (see include/mla_sparse.h); indices: int32
     [B, q_len, topk] token positions, -1 = unused."""
     _check_cuda(q_nope, q_pe, kv_cache, page_table, seq_lens, indices, out, lse, workspace)
+    _check_decode_tensors(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace)
+    _check_indices(indices, q_nope)
     B, Q, topk = indices.shape
-    if (B, Q) != tuple(q_nope.shape[:2]) or not indices.is_contiguous():
-        raise ValueError("indices must be a contiguous [B, q_len, topk] tensor")
     dims = make_dims(q_nope, kv_cache, page_table)
     rc = load_library().mla_decode_sparse(
         ctypes.byref(dims), _ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(page_table), _ptr(seq_lens),
@@ -330,6 +422,7 @@ def mla_decode_cascade(q_nope, q_pe, kv_cache, page_table, seq_lens, prefix_page
                        workspace, stream=None) -> None:
     """Enqueue a cascade decode over a shared prefix (see include/mla_cascade.h)."""
     _check_cuda(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace)
+    _check_decode_tensors(q_nope, q_pe, kv_cache, page_table, seq_lens, out, lse, workspace)
     dims = make_dims(q_nope, kv_cache, page_table)
     rc = load_library().mla_decode_cascade(
         ctypes.byref(dims), _ptr(q_nope), _ptr(q_pe), _ptr(kv_cache), _ptr(page_table), _ptr(seq_lens),

@@ -183,3 +183,76 @@ def test_sparse_and_cascade_reject_before_the_device(lib):
     assert lib.mla_decode_cascade(ctypes.byref(d), *args, 2, 3, 1.0, 1.0, P, P, P, 1 << 30, None) == -1  # q_len
     W = ctypes.c_void_p(256 + 64)
     assert lib.mla_decode_cascade(ctypes.byref(d), *args, 2, 1, 1.0, 1.0, P, P, W, 1 << 30, None) == -3
+
+
+# ---- the binding's layout checks (run on CPU tensors: the checks look only
+# at shapes, element types and strides; the CUDA check comes before them) ----
+
+def _decode_tensors(kv_dtype="bf16", Q=2):
+    torch = pytest.importorskip("torch")
+    from paged_mla_decode_09_gb300 import workloads as W
+    from paged_mla_decode_09_gb300.device_inputs import to_device
+
+    wl = W.custom([100, 70], num_heads=16, q_len=Q, kv_dtype=kv_dtype, seed=3)
+    db = to_device(wl, "cpu")
+    B, H = wl.batch, wl.num_heads
+    t = dict(q_nope=db.q_nope, q_pe=db.q_pe, kv_cache=db.kv_cache, page_table=db.page_table, seq_lens=db.seq_lens,
+             out=torch.empty(B, Q, H, 512, dtype=torch.bfloat16), lse=torch.empty(B, Q, H, dtype=torch.float32),
+             workspace=torch.empty(4096, dtype=torch.uint8))
+    return torch, wl, t
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_layout_checks_accept_what_the_tests_pass(kv_dtype):
+    torch, wl, t = _decode_tensors(kv_dtype)
+    mla._check_decode_tensors(**t)
+    # a page table that is a column slice of a wider one keeps unit column stride
+    wide = torch.full((wl.batch, wl.max_pages + 3), -1, dtype=torch.int32)
+    wide[:, :wl.max_pages] = t["page_table"]
+    mla._check_decode_tensors(**{**t, "page_table": wide[:, :wl.max_pages]})
+    idx = torch.from_numpy(__import__("paged_mla_decode_09_gb300.workloads", fromlist=["x"]).topk_indices(wl, 8, 1))
+    mla._check_indices(idx, t["q_nope"])
+
+
+def _bad_variants(torch, t):
+    B, Q, H, _ = t["q_nope"].shape
+    yield "q_nope", t["q_nope"][:1].expand(B, Q, H, 512)          # broadcast view: smaller storage
+    yield "q_nope", t["q_nope"].float()
+    yield "q_pe", t["q_pe"][..., :32]
+    yield "out", torch.empty(B, Q, 512, H, dtype=torch.bfloat16).transpose(2, 3)
+    yield "lse", torch.empty(B, Q, H, dtype=torch.bfloat16)
+    yield "seq_lens", t["seq_lens"].long()
+    yield "page_table", t["page_table"].long()
+    yield "page_table", t["page_table"].t().contiguous().t()       # column-major
+    yield "page_table", t["page_table"][:1]
+    yield "kv_cache", t["kv_cache"][..., :512]
+    yield "kv_cache", t["kv_cache"].float() if t["kv_cache"].dtype == torch.bfloat16 else t["kv_cache"].short()
+    yield "workspace", torch.empty(64, 2, dtype=torch.uint8).t()
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_layout_checks_reject_mismatched_tensors(case):
+    torch, wl, t = _decode_tensors()
+    name, bad = list(_bad_variants(torch, t))[case]
+    with pytest.raises((ValueError, TypeError)):
+        mla._check_decode_tensors(**{**t, name: bad})
+
+
+def test_index_and_cache_write_layout_checks():
+    torch, wl, t = _decode_tensors()
+    good = torch.zeros(wl.batch, wl.q_len, 8, dtype=torch.int32)
+    mla._check_indices(good, t["q_nope"])
+    for bad in (good.long(), good[:1], good.transpose(1, 2).contiguous().transpose(1, 2), good[..., None]):
+        with pytest.raises(ValueError):
+            mla._check_indices(bad, t["q_nope"])
+    # the cache write, with the tensors its tests build
+    rows = torch.zeros(wl.batch, 2, 576, dtype=torch.bfloat16)
+    cache = torch.zeros(8, 64, 576, dtype=torch.uint8)
+    status = torch.zeros(1, dtype=torch.int32)
+    mla._check_kv_pack_tensors(rows, t["page_table"], t["seq_lens"], cache, status)
+    for args in ((rows.view(torch.int16), t["page_table"], t["seq_lens"], cache, status),
+                 (rows, t["page_table"], t["seq_lens"], cache, status.long()),
+                 (rows, t["page_table"].long(), t["seq_lens"], cache, status),
+                 (rows[:, :, :512], t["page_table"], t["seq_lens"], cache, status)):
+        with pytest.raises(ValueError):
+            mla._check_kv_pack_tensors(*args)
