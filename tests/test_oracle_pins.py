@@ -515,3 +515,97 @@ def test_sparse_bad_entries_are_flagged_and_skipped():
     o, l, st = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, empty,
                                             wl.scale, requests=[1])
     assert st == oracle.sparse.BAD_INDEX and np.all(o[1] == 0) and np.all(l[1] == 0)
+
+
+# ------------------------------------------------- properties (hypothesis)
+# Randomised statements of the same mathematics: any partition of the keys
+# merges back to the unsplit result; the merge is order-free; a rope term
+# that scores every key alike moves lse and leaves out alone.
+
+def _hyp():
+    return pytest.importorskip("hypothesis")
+
+
+def test_property_any_partition_merges_to_unsplit():
+    hyp = _hyp()
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=25, deadline=None, derandomize=True)
+    @hyp.given(L=st.integers(1, 200), Q=st.integers(1, 3), H=st.integers(1, 3), data=st.data())
+    def check(L, Q, H, data):
+        L = max(L, Q)
+        wl = W.custom([L], num_heads=H, q_len=Q, seed=L * 7 + Q * 3 + H)
+        inner = data.draw(st.lists(st.integers(1, L - 1), max_size=6, unique=True)) if L > 1 else []
+        cuts = [[0] + sorted(inner) + [L]]
+        a = mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, Q, wl.scale)
+        b = mla_decode_ref_pieces(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, Q, wl.scale, cuts)
+        np.testing.assert_allclose(b[0], a[0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(b[1], a[1], rtol=0, atol=1e-12)
+
+    check()
+
+
+def test_property_lse_merge_is_order_free_and_associative():
+    hyp = _hyp()
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=50, deadline=None, derandomize=True)
+    @hyp.given(seed=st.integers(0, 10**6), n=st.integers(2, 5), empty=st.integers(-1, 4))
+    def check(seed, n, empty):
+        rng = np.random.default_rng(seed)
+        outs = rng.standard_normal((n, 3, 8))
+        lses = rng.uniform(-30, 30, size=(n, 3))
+        if 0 <= empty < n:
+            lses[empty] = -np.inf
+            outs[empty] = 0.0
+        o, l = lse_merge(outs, lses)
+        perm = rng.permutation(n)
+        op, lp = lse_merge(outs[perm], lses[perm])
+        np.testing.assert_allclose(op, o, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lp, l, rtol=1e-12, atol=1e-12)
+        k = n // 2  # merge the first k, then the rest
+        with np.errstate(divide="ignore"):  # a half holding only the empty piece merges to lse = -inf
+            o1, l1 = lse_merge(outs[:k], lses[:k])
+            o2, l2 = lse_merge(outs[k:], lses[k:])
+        oc, lc = lse_merge(np.stack([o1, o2]), np.stack([l1, l2]))
+        np.testing.assert_allclose(oc, o, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lc, l, rtol=1e-12, atol=1e-12)
+
+    check()
+
+
+def test_property_uniform_rope_term_shifts_lse_only():
+    hyp = _hyp()
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=15, deadline=None, derandomize=True)
+    @hyp.given(L=st.integers(1, 150), H=st.integers(1, 4), seed=st.integers(0, 1000))
+    def check(L, H, seed):
+        wl = W.custom([L], num_heads=H, q_len=1, seed=seed)
+        cache = wl.kv_cache.copy()
+        k_pe = cache[wl.page_table[0, 0], 0, 512:].copy()
+        for j in range((L + 63) // 64):  # every visible key gets the same k_pe
+            cache[wl.page_table[0, j], :, 512:] = k_pe
+        zero_pe = np.zeros_like(wl.q_pe)  # bf16 bits of +0.0
+        a_out, a_lse = mla_decode_ref(wl.q_nope, wl.q_pe, cache, wl.page_table, wl.seq_lens, 1, wl.scale)
+        b_out, b_lse = mla_decode_ref(wl.q_nope, zero_pe, cache, wl.page_table, wl.seq_lens, 1, wl.scale)
+        shift = wl.scale * (oracle.bf16_bits_to_f64(wl.q_pe[0, 0]) @ oracle.bf16_bits_to_f64(k_pe))  # [H]
+        np.testing.assert_allclose(a_out, b_out, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(a_lse[0, 0], b_lse[0, 0] + shift, rtol=1e-12, atol=1e-10)
+
+    check()
+
+
+def test_property_e4m3_encoder_is_monotone():
+    hyp = _hyp()
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=40, deadline=None, derandomize=True)
+    @hyp.given(xs=st.lists(st.floats(-600, 600, allow_nan=False, width=32), min_size=2, max_size=64))
+    def check(xs):
+        x = np.sort(np.asarray(xs, dtype=np.float32))
+        v = oracle.e4m3_to_f64(oracle.e4m3_encode(x))
+        assert np.all(np.diff(v) >= 0)
+        assert np.all(np.abs(v) <= 448)
+
+    check()
