@@ -256,3 +256,22 @@ def test_index_and_cache_write_layout_checks():
                  (rows[:, :, :512], t["page_table"], t["seq_lens"], cache, status)):
         with pytest.raises(ValueError):
             mla._check_kv_pack_tensors(*args)
+
+
+def test_binding_constants_match_the_headers():
+    """Every MLA_* constant the binding defines has the value the C headers
+    give it (status codes, device status bits, cache types)."""
+    vals = {}
+    for fname in os.listdir(os.path.join(ROOT, "include")):
+        if fname.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", fname)).read(), flags=re.S)
+            for name, v in re.findall(r"\b(MLA_[A-Z0-9_]+)\s*=\s*(-?\d+)", text):
+                vals[name] = int(v)
+    mine = {k: getattr(mla, k) for k in dir(mla) if re.fullmatch(r"MLA_[A-Z0-9_]+", k) and isinstance(getattr(mla, k), int)}
+    assert mine, "the binding defines no constants"
+    for k, v in mine.items():
+        assert k in vals, f"{k} is not declared in include/"
+        assert vals[k] == v, f"{k}: binding {v}, header {vals[k]}"
+    # the device status bits are distinct powers of two
+    bits = [v for k, v in vals.items() if k.startswith("MLA_DEV_")]
+    assert len(set(bits)) == len(bits) and all(b > 0 and b & (b - 1) == 0 for b in bits)
