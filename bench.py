@@ -18,6 +18,15 @@ prefill (64 requests x 4096 new tokens) into an e4m3 cache; metric rows/s.
 Prints one JSON line (rank 0).  With N > 1 (torchrun, one rank per GPU)
 every rank decodes its own replica of the batch (requests are independent,
 so the path shards by request with no collective: weak scaling).
+
+Timing: W untimed warm-up steps, then K steps, each between two CUDA events
+on the launching stream; between steps the L2 is flushed (512 MiB written,
+then read back).  ``value`` is whole-job throughput with inputs resident in
+HBM; ``e2e`` is the same metric through the public call with host buffers
+(inputs up, out and lse down, pipelined on two copy streams);
+``roofline`` compares the dominant kernel's algorithmic bytes or FLOPs per
+launch, over its event-timed duration, with the measured peaks;
+``cpu_baseline`` times the float64 oracle on a bounded sample on the host.
 """
 from __future__ import annotations
 
