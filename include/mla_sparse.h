@@ -54,6 +54,8 @@ size_t mla_decode_sparse_workspace_size(const mla_dims* d, int32_t topk, int dev
  *               alignment and errors)
  *   indices     int32 [B][q_len][topk] token positions (device), 4-byte aligned
  *   topk        entries per (b, i), 1 .. 65536
+ *   B * q_len   at most 65535 (MLA_ERR_UNSUPPORTED beyond; the workspace
+ *               size is then 0)
  *   workspace   device, 256-byte aligned, at least
  *               mla_decode_sparse_workspace_size(d, topk) bytes
  *

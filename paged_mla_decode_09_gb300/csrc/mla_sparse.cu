@@ -19,6 +19,7 @@ namespace {
 
 constexpr int kPageRows = 64;
 constexpr int kChunkEntries = 256;  // top-k entries per gather block
+constexpr int64_t kMaxPacked = 65535;  // (b, i) pairs: the gather grid's y extent
 constexpr int kRowsInFlight = 2;    // rows a warp copies per round (all loads first; 1-8 measured, 1-2 best)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -152,7 +153,7 @@ bool packed_dims(const mla_dims* d, int32_t topk, mla_dims* pd) {
   if (d->batch < 1 || d->q_len < 1 || d->num_heads < 1) return false;
   const int64_t bq = static_cast<int64_t>(d->batch) * d->q_len;
   const int64_t p_per = (topk + kPageRows - 1) / kPageRows;
-  if (bq * p_per > INT_MAX / kPageRows) return false;
+  if (bq > kMaxPacked || bq * p_per > INT_MAX / kPageRows) return false;
   *pd = *d;
   pd->batch = static_cast<int32_t>(bq);
   pd->q_len = 1;
@@ -202,6 +203,7 @@ int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, c
   if (!aligned(indices, 4) || !aligned(workspace, 256) || !aligned(kv_cache, 16) || !aligned(page_table, 4) ||
       !aligned(seq_lens, 4))
     return MLA_ERR_ALIGNMENT;
+  if (static_cast<int64_t>(d->batch) * d->q_len > kMaxPacked) return MLA_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
   SparseLayout l;

@@ -179,6 +179,9 @@ def test_sparse_and_cascade_reject_before_the_device(lib):
                                  None) == -2
     M = ctypes.c_void_p(258)
     assert lib.mla_decode_sparse(ctypes.byref(d), *args, M, 8, 1, 1.0, 1.0, P, P, P, 1 << 30, None) == -3
+    big = _dims(batch=70000)  # more (request, draft) pairs than the gather grid holds
+    assert lib.mla_decode_sparse(ctypes.byref(big), *args, P, 8, 1, 1.0, 1.0, P, P, P, 1 << 30, None) == -2
+    assert lib.mla_decode_sparse_workspace_size(ctypes.byref(big), 8, 0) == 0
     assert lib.mla_decode_cascade(ctypes.byref(d), *args, 2, 1, 1.0, 1.0, P, P, None, 1 << 30, None) == -1
     assert lib.mla_decode_cascade(ctypes.byref(d), *args, 2, 3, 1.0, 1.0, P, P, P, 1 << 30, None) == -1  # q_len
     W = ctypes.c_void_p(256 + 64)
