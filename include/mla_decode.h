@@ -73,7 +73,9 @@ typedef struct {
   int32_t q_len;             /* draft positions per request; H*q_len <= 256 */
   int32_t page_size;         /* must be 64 */
   int32_t num_pages;         /* pool size; valid page ids are [0, num_pages) */
-  int32_t max_pages_per_req; /* columns of the page table a request may use */
+  int32_t max_pages_per_req; /* columns of the page table a request may use; max_pages_per_req * 64
+                                and batch * max_pages_per_req must fit in int32 (else
+                                MLA_ERR_UNSUPPORTED) */
   int32_t page_table_stride; /* int32 elements between page-table rows (>= max_pages_per_req) */
   int32_t kv_dtype;          /* mla_kv_dtype */
 } mla_dims;
@@ -139,6 +141,7 @@ int mla_query_status(const void* workspace, void* stream, int32_t* device_status
  * the same tensor-map TMA page loads as the decode kernel.  `row_offsets`
  * is int64 [B+1] (device) with row_offsets[b] = sum_{c<b} seq_lens[c].
  * Device errors go to the status word of `workspace` (>= 256 bytes).
+ * batch > 65535 is refused (MLA_ERR_UNSUPPORTED) before anything is enqueued.
  */
 int mla_gather_rows(const mla_dims* d, const void* kv_cache, const int32_t* page_table,
                     const int32_t* seq_lens, const int64_t* row_offsets, void* rows_out,
@@ -165,9 +168,16 @@ int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream
  * outputs.  Nothing is allocated or freed.
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
+ *     A device reset (cudaDeviceReset, a primary-context reset) loads the
+ *     library's device code again: the next call looks the address up
+ *     again, so it too belongs outside a capture.
  *   - The call runs on fewer clusters when the split partials of all the
- *     device's clusters would not fit in 16 MiB; if even one cluster's do
- *     not (very large batches), it returns MLA_ERR_SCRATCH_TOO_SMALL.
+ *     device's clusters would not fit in 16 MiB (each cluster needs about
+ *     G * 0.5 MiB, G = ceil(num_heads * q_len / 128): at most about 31
+ *     clusters with G = 1 and 15 with G = 2, against 76 and 36 for
+ *     mla_decode on GB300), so large batches decode more slowly than with
+ *     mla_decode; if even one cluster's partials do not fit (very large
+ *     batches), it returns MLA_ERR_SCRATCH_TOO_SMALL.
  *   - All calls share the one array, which keeps the last call's contents:
  *     calls that may overlap on the GPU (other streams, other threads)
  *     race and must be serialised by the caller.

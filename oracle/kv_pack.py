@@ -8,13 +8,19 @@ of length L holds its tokens at positions 0 .. L - 1, position t in slot
 t % 64 of page page_table[b][t // 64], and the step's num_new new tokens
 are the last num_new positions (they are already counted in L).
 
-Readings where the pages are silent (also listed in the design doc):
+The quantisation itself follows the guijiagi.com "推理优化" tag page,
+quantisation article (三大量化方案原理 > INT8量化): a value is quantised as
+round(value / scale) and dequantised as scale * code.  Here the grid is
+e4m3's, so the code is the e4m3 value nearest to x / kv_scale (ties to the
+even code, saturated to +-448; see e4m3.e4m3_encode), kv_scale taken as the
+fp32 number the C entry point receives.  x / kv_scale is formed in float64:
+x has 8 significant bits, kv_scale 24 and an e4m3 midpoint 5, so x / kv_scale
+is either exactly a midpoint or at least 2**-38 of it away (relative), far
+beyond float64's 2**-53 rounding; the float64 quotient therefore rounds to
+the same code as the exact quotient.
 
-* e4m3 code = e4m3(x * r) with r = 1 / kv_scale rounded to fp32 and x * r
-  the fp32 product (rounded to nearest-even) of the bf16 value and r, then
-  rounded to nearest-even e4m3 and saturated (see e4m3.e4m3_encode):
-  scaling by a reciprocal is the plainest way to apply one per-tensor scale
-  to every value; decoding multiplies by kv_scale, as the decode does;
+Readings where the pages are silent:
+
 * a bf16 cache receives the row unchanged;
 * a row whose page id is outside the pool, or whose sequence length is
   outside [num_new, max_pages * 64], is not written and raises a flag
@@ -35,6 +41,13 @@ BAD_SEQ_LEN = 2
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) to the float32 values they denote."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def quantise_e4m3(rows_bits: np.ndarray, kv_scale: float) -> np.ndarray:
+    """e4m3 codes of bf16 values (uint16 bits, any shape): the code nearest to
+    x / kv_scale, kv_scale taken as an fp32 number."""
+    x = bf16_bits_to_f32(rows_bits).astype(np.float64)
+    return e4m3_encode(x / np.float64(np.float32(kv_scale)))
 
 
 def kv_pack_ref(rows_bits: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray, kv_scale: float,
@@ -63,9 +76,7 @@ def kv_pack_ref(rows_bits: np.ndarray, page_table: np.ndarray, seq_lens: np.ndar
             if kv_dtype == "bf16":
                 cache[page, t % page_size] = rows_bits[b, i]
             elif kv_dtype == "fp8_e4m3":
-                r = np.float32(1.0) / np.float32(kv_scale)  # fp32 reciprocal
-                scaled = bf16_bits_to_f32(rows_bits[b, i]) * r  # fp32 products
-                cache[page, t % page_size] = e4m3_encode(scaled.astype(np.float32))
+                cache[page, t % page_size] = quantise_e4m3(rows_bits[b, i], kv_scale)
             else:
                 raise ValueError(kv_dtype)
     return cache, status

@@ -18,7 +18,7 @@ Sources (page title and section):
 * Same tag page, KV-cache article (PagedAttention): the cache is cut into
   fixed-size blocks addressed through a per-request page table.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * the log-sum-exp is the natural log of sum(exp(score)), score including the
   softmax scale;

@@ -7,7 +7,7 @@ not part of this operation; its output (token positions per request and
 draft position) is an input.  The attention over the picked rows is the
 plain decode of mla_oracle (softmax over the picked keys only).
 
-Readings where the pages are silent (also listed in the design doc):
+Readings where the pages are silent:
 
 * an entry t is used when 0 <= t < n, n = seq_len - q_len + i + 1 (the
   causal visibility of draft i); -1 means unused; any other entry is

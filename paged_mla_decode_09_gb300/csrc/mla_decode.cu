@@ -65,6 +65,10 @@ int check_dims(const mla_dims* d) {
   if (d->kv_dtype != MLA_KV_BF16 && d->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->num_heads) * d->q_len > 256) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->num_pages) * 64 > (1ll << 31) - 1) return MLA_ERR_UNSUPPORTED;
+  // token positions of one request and the schedule's page prefix sums over
+  // all requests are int32 on the device
+  if (static_cast<int64_t>(d->max_pages_per_req) * 64 > (1ll << 31) - 1) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->batch) * d->max_pages_per_req > (1ll << 31) - 1) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
 }
 
@@ -214,21 +218,39 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
-int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
-                const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
-                void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream_v,
-                void* const* events) {
+// The launch sequence of both decode entry points.  `ws` is the scratch
+// (status words, schedule, split partials): the caller's workspace for
+// mla_decode, the library's static array for mla_decode_noalloc.  With
+// shrink_to_fit the attention kernel runs on fewer clusters when the split
+// partials of every cluster the device could hold would not fit in
+// ws_bytes (none at all: MLA_ERR_SCRATCH_TOO_SMALL); without it a workspace
+// below the full size is MLA_ERR_WORKSPACE_TOO_SMALL.  status_out (device,
+// may be null) receives a copy of the status word at the end, on `stream`.
+// Checks of a decode call's arguments that need no device.
+int check_call(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+               const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
+               const void* out, const float* lse, const int32_t* status_out) {
   int rc = check_dims(d);
   if (rc != MLA_OK) return rc;
   if (q_len != d->q_len) return MLA_ERR_INVALID_ARG;
-  if (!q_nope || !q_pe || !kv_cache || !page_table || !seq_lens || !out || !lse || !workspace)
-    return MLA_ERR_INVALID_ARG;
+  if (!q_nope || !q_pe || !kv_cache || !page_table || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
   // the softmax scale (and an e4m3 cache's scale) must be positive and finite
   if (!(scale > 0.f) || scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
   if (d->kv_dtype == MLA_KV_FP8_E4M3 && (!(kv_scale > 0.f) || kv_scale > 3.0e38f)) return MLA_ERR_INVALID_ARG;
   if (!aligned(q_nope, 32) || !aligned(q_pe, 32) || !aligned(kv_cache, 16) || !aligned(out, 32) ||
-      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) || (status_out && !aligned(status_out, 4)))
     return MLA_ERR_ALIGNMENT;
+  return MLA_OK;
+}
+
+int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+                const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
+                void* out, float* lse, uint8_t* ws, size_t ws_bytes, bool shrink_to_fit, int32_t* status_out,
+                void* stream_v, void* const* events) {
+  int rc = check_call(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, status_out);
+  if (rc != MLA_OK) return rc;
+  if (!ws) return MLA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MLA_ERR_ALIGNMENT;
   int dev = 0;
   if ((rc = current_device(&dev)) != MLA_OK) return rc;
   if ((rc = device_ok(dev)) != MLA_OK) return rc;
@@ -237,13 +259,16 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   const int G = (R + mla::kRows - 1) / mla::kRows;
   int C = 0;
   if ((rc = launch_shape(dev, f8, G, &C)) != MLA_OK) return rc;
+  if (shrink_to_fit) {
+    while (C > 0 && workspace_layout(d->batch, C, G).total > ws_bytes) --C;
+    if (C < 1) return MLA_ERR_SCRATCH_TOO_SMALL;
+  }
   const Layout lay = workspace_layout(d->batch, C, G);
-  if (workspace_bytes < lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   Maps maps;
   if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
   if ((rc = make_qmaps(q_nope, q_pe, static_cast<int64_t>(d->batch) * R, &maps)) != MLA_OK) return rc;
 
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   Params p;
   p.q_nope = static_cast<const uint8_t*>(q_nope);
   p.q_pe = static_cast<const uint8_t*>(q_pe);
@@ -317,6 +342,8 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
     return MLA_ERR_CUDA;
   }
   if (!mark(3)) return MLA_ERR_CUDA;
+  if (status_out && cudaMemcpyAsync(status_out, p.status, 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
@@ -362,8 +389,8 @@ size_t mla_decode_workspace_size(const mla_dims* d, int device) {
 int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
                const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
                void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, workspace,
-                     workspace_bytes, stream, nullptr);
+  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse,
+                     static_cast<uint8_t*>(workspace), workspace_bytes, false, nullptr, stream, nullptr);
 }
 
 int mla_decode_profiled(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
@@ -371,8 +398,8 @@ int mla_decode_profiled(const mla_dims* d, const void* q_nope, const void* q_pe,
                         float kv_scale, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
                         void* const* events) {
   if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return MLA_ERR_INVALID_ARG;
-  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, workspace,
-                     workspace_bytes, stream, events);
+  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse,
+                     static_cast<uint8_t*>(workspace), workspace_bytes, false, nullptr, stream, events);
 }
 
 int mla_query_status(const void* workspace, void* stream_v, int32_t* device_status) {
@@ -391,6 +418,7 @@ int mla_gather_rows(const mla_dims* d, const void* kv_cache, const int32_t* page
   if (!kv_cache || !page_table || !seq_lens || !row_offsets || !rows_out || !workspace) return MLA_ERR_INVALID_ARG;
   if (!aligned(kv_cache, 16) || !aligned(rows_out, 16) || !aligned(workspace, 256) || !aligned(row_offsets, 8))
     return MLA_ERR_ALIGNMENT;
+  if (d->batch > 65535) return MLA_ERR_UNSUPPORTED;  // the grid's y extent; refused before anything is enqueued
   int dev = 0;
   if ((rc = current_device(&dev)) != MLA_OK) return rc;
   if ((rc = device_ok(dev)) != MLA_OK) return rc;
@@ -455,24 +483,55 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device with that
-// device current (in host code the symbol itself is only a stand-in).
+// Device address of g_noalloc_scratch, looked up with the device current (in
+// host code the symbol itself is only a stand-in).  It is cached per device
+// together with the id of the context it was found in: a device reset
+// (cudaDeviceReset, a primary-context reset) creates a new context in which
+// the module, and this array, are loaded again, possibly elsewhere, and the
+// next call then looks the address up again.
 struct NoAllocScratch {
   std::mutex mu;
   void* ptr[64] = {};
+  unsigned long long ctx_id[64] = {};
 };
 NoAllocScratch g_noalloc;
 
+// Id of the current context (unique within the process, never reused), or 0
+// when there is none yet or the driver cannot be asked.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 int noalloc_scratch(int device, uint8_t** out) {
   if (device < 0 || device >= 64) return MLA_ERR_INVALID_ARG;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lk(g_noalloc.mu);
-  if (!g_noalloc.ptr[device]) {
+  if (!g_noalloc.ptr[device] || id == 0 || g_noalloc.ctx_id[device] != id) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
       cudaGetLastError();
       return MLA_ERR_CUDA;
     }
     g_noalloc.ptr[device] = ptr;
+    g_noalloc.ctx_id[device] = current_context_id();  // the lookup made the context current if it was not
   }
   *out = static_cast<uint8_t*>(g_noalloc.ptr[device]);
   return MLA_OK;
@@ -482,107 +541,18 @@ int noalloc_scratch(int device, uint8_t** out) {
 
 extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
                                   const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale,
-                                  float kv_scale, void* out, float* lse, int32_t* status_out, void* stream_v) {
-  int rc = check_dims(d);
+                                  float kv_scale, void* out, float* lse, int32_t* status_out, void* stream) {
+  int rc = check_call(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, status_out);
   if (rc != MLA_OK) return rc;
-  if (q_len != d->q_len) return MLA_ERR_INVALID_ARG;
-  if (!q_nope || !q_pe || !kv_cache || !page_table || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
-  if (d->kv_dtype == MLA_KV_FP8_E4M3 && (!(kv_scale > 0.f) || kv_scale > 3.0e38f)) return MLA_ERR_INVALID_ARG;
-  if (!aligned(q_nope, 32) || !aligned(q_pe, 32) || !aligned(kv_cache, 16) || !aligned(out, 32) ||
-      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
-      (status_out && !aligned(status_out, 4)))
-    return MLA_ERR_ALIGNMENT;
   int dev = 0;
   if ((rc = current_device(&dev)) != MLA_OK) return rc;
   if ((rc = device_ok(dev)) != MLA_OK) return rc;
-  const bool f8 = d->kv_dtype == MLA_KV_FP8_E4M3;
-  const int R = d->num_heads * d->q_len;
-  const int G = (R + mla::kRows - 1) / mla::kRows;
-  int C = 0;
-  if ((rc = launch_shape(dev, f8, G, &C)) != MLA_OK) return rc;
-  // Fewer clusters than the device could hold when the split partials of all
-  // of them would not fit in the fixed scratch; none at all is an error.
-  while (C > 0 && workspace_layout(d->batch, C, G).total > kNoAllocScratchBytes) --C;
-  if (C < 1) return MLA_ERR_SCRATCH_TOO_SMALL;
-  const Layout lay = workspace_layout(d->batch, C, G);
   uint8_t* ws = nullptr;
   if ((rc = noalloc_scratch(dev, &ws)) != MLA_OK) return rc;
-  Maps maps;
-  if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
-  if ((rc = make_qmaps(q_nope, q_pe, static_cast<int64_t>(d->batch) * R, &maps)) != MLA_OK) return rc;
-
-  Params p;
-  p.q_nope = static_cast<const uint8_t*>(q_nope);
-  p.q_pe = static_cast<const uint8_t*>(q_pe);
-  p.page_table = page_table;
-  p.seq_lens = seq_lens;
-  p.out = static_cast<uint8_t*>(out);
-  p.lse = lse;
-  p.o_part = reinterpret_cast<float*>(ws + lay.o_part);
-  p.lse_part = reinterpret_cast<float*>(ws + lay.lse_part);
-  p.status = reinterpret_cast<int32_t*>(ws + lay.status);
-  p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
-  p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
-  p.rrange = reinterpret_cast<int32_t*>(ws + lay.rrange);
-  p.qscale = reinterpret_cast<float*>(ws + lay.qscale);
-  p.B = d->batch;
-  p.H = d->num_heads;
-  p.Q = d->q_len;
-  p.R = R;
-  p.G = G;
-  p.C = C;
-  p.num_pages = d->num_pages;
-  p.max_pages = d->max_pages_per_req;
-  p.pt_stride = d->page_table_stride;
-  p.unit_cost = mla::unit_cost_pages(f8, R < mla::kRows ? R : mla::kRows);
-  p.scale = scale;
-  p.kv_scale = f8 ? kv_scale : 1.f;
-  p.timeout_ns = kTimeoutNs;
-
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
-  // the status words must start at zero; everything else in the scratch is
-  // written before it is read within the call
-  if (cudaMemsetAsync(p.status, 0, 16, stream) != cudaSuccess) return MLA_ERR_CUDA;
-  mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
-  if (f8) {
-    if (launch_pdl(mla::mla_qscale_kernel, dim3(static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8)),
-                   dim3(256), stream, p) != cudaSuccess) {
-      cudaGetLastError();
-      return MLA_ERR_CUDA;
-    }
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * G * C, 1, 1);
-  cfg.blockDim = dim3(mla::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = f8 ? Cfg<true>::kSmem : Cfg<false>::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2 * G;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // prologue overlaps the schedule
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe, maps.qn,
-                                          maps.qp)
-                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe,
-                                          maps.qn, maps.qp);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return MLA_ERR_CUDA;
-  }
-  if (launch_pdl(mla::mla_combine_kernel, dim3(d->batch, G, mla::kRows / 8), dim3(256), stream, p) != cudaSuccess) {
-    cudaGetLastError();
-    return MLA_ERR_CUDA;
-  }
-  if (status_out &&
-      cudaMemcpyAsync(status_out, p.status, 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-    return MLA_ERR_CUDA;
-  return MLA_OK;
+  // the status words start at zero (decode_impl clears them); everything
+  // else in the scratch is written before it is read within the call
+  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, ws,
+                     kNoAllocScratchBytes, true, status_out, stream, nullptr);
 }
 
 #ifdef MLA_TRACE

@@ -7,6 +7,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -28,12 +29,42 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const uint4* p) {
   return v;
 }
 
+// e4m3 code nearest to x / scale when x * inv_scale * (1 - 2^-20) rounds to
+// code ca and x * inv_scale * (1 + 2^-20) to code cb != ca: the two codes are
+// neighbours and the quotient lies on one side of their midpoint m, or on
+// it.  x - m * scale has the sign of (x / scale - m) for scale > 0, and one
+// fma gives that sign exactly (one rounding never changes a sign; only an
+// exact zero is zero).  A tie goes to the even code (mantissa bit 0 clear).
+__device__ __noinline__ uint32_t e4m3_resolve(uint32_t ca, uint32_t cb, float x, float scale) {
+  const float va = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(ca), __NV_E4M3)));
+  const float vb = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(cb), __NV_E4M3)));
+  const float m = 0.5f * (va + vb);  // exact: neighbouring e4m3 values have at most 5 significant bits together
+  const float t = __fmaf_rn(-m, scale, x);
+  if (t > 0.f) return va > vb ? ca : cb;
+  if (t < 0.f) return va > vb ? cb : ca;
+  return (ca & 1u) ? cb : ca;
+}
+
 // e4m3 codes of two bf16 values (packed as in memory, the lower address in
-// the low half) times 1 / kv_scale: the lower address goes to the low byte
-__device__ __forceinline__ uint32_t e4m3x2(uint32_t bf2, float inv_scale) {
+// the low half) divided by kv_scale: the nearest code to the exact quotient
+// x / kv_scale, ties to even, saturated to +-448.  The quotient is
+// bracketed without a division: with r = fp32(1 / kv_scale), x * r is
+// within 2^-23 (relative) of x / kv_scale, so x * r * (1 -+ 2^-20) lie on
+// either side of it; when both round to the same code, so does the
+// quotient (rounding is monotone), and otherwise (a midpoint within about
+// 2^-20 of the quotient: rare) e4m3_resolve decides.
+__device__ __forceinline__ uint32_t e4m3x2(uint32_t bf2, float inv_scale, float scale) {
   const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bf2));
-  const float2 y = make_float2(__fmul_rn(x.x, inv_scale), __fmul_rn(x.y, inv_scale));
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3));
+  const float q0 = __fmul_rn(x.x, inv_scale), q1 = __fmul_rn(x.y, inv_scale);
+  constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+  const uint32_t lo = static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(q0, kDown), __fmul_rn(q1, kDown)), __NV_SATFINITE, __NV_E4M3));
+  const uint32_t hi = static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(q0, kUp), __fmul_rn(q1, kUp)), __NV_SATFINITE, __NV_E4M3));
+  if (lo == hi) return lo;
+  const uint32_t c0 = (lo & 0xFFu) == (hi & 0xFFu) ? (lo & 0xFFu) : e4m3_resolve(lo & 0xFFu, hi & 0xFFu, x.x, scale);
+  const uint32_t c1 = (lo >> 8) == (hi >> 8) ? (lo >> 8) : e4m3_resolve(lo >> 8, hi >> 8, x.y, scale);
+  return c0 | (c1 << 8);
 }
 
 }  // namespace
@@ -44,7 +75,7 @@ template <bool kF8>
 __global__ void __launch_bounds__(kWarps * 32)
     mla_kv_pack_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ page_table,
                        const int32_t* __restrict__ seq_lens, int batch, int num_new, int num_pages, int max_pages,
-                       int stride, float inv_scale, uint8_t* __restrict__ cache, int32_t* status) {
+                       int stride, float inv_scale, float scale, uint8_t* __restrict__ cache, int32_t* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   if (row >= static_cast<int64_t>(batch) * num_new) return;
@@ -74,8 +105,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       if (lane + 32 * k >= kChunks) break;
-      const uint32_t lo = e4m3x2(v[k].x, inv_scale) | (e4m3x2(v[k].y, inv_scale) << 16);
-      const uint32_t hi = e4m3x2(v[k].z, inv_scale) | (e4m3x2(v[k].w, inv_scale) << 16);
+      const uint32_t lo = e4m3x2(v[k].x, inv_scale, scale) | (e4m3x2(v[k].y, inv_scale, scale) << 16);
+      const uint32_t hi = e4m3x2(v[k].z, inv_scale, scale) | (e4m3x2(v[k].w, inv_scale, scale) << 16);
       dst[lane + 32 * k] = make_uint2(lo, hi);
     }
   } else {
@@ -102,7 +133,9 @@ extern "C" int mla_kv_pack(const mla_kv_pack_dims* d, const void* rows, const in
     return MLA_ERR_INVALID_ARG;
   if (d->kv_dtype != MLA_KV_BF16 && d->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
   const bool f8 = d->kv_dtype == MLA_KV_FP8_E4M3;
-  if (f8 && !(kv_scale > 0.f && std::isfinite(kv_scale))) return MLA_ERR_INVALID_ARG;
+  // a normal, finite scale whose reciprocal is finite too
+  if (f8 && !(kv_scale >= FLT_MIN && std::isfinite(kv_scale) && std::isfinite(1.0f / kv_scale)))
+    return MLA_ERR_INVALID_ARG;
   if (!aligned(rows, 16) || !aligned(kv_cache, 16) || !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
       !aligned(status, 4))
     return MLA_ERR_ALIGNMENT;
@@ -117,16 +150,16 @@ extern "C" int mla_kv_pack(const mla_kv_pack_dims* d, const void* rows, const in
     return MLA_ERR_CUDA;
   if (major != 10 || minor != 3) return MLA_ERR_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const float inv_scale = f8 ? 1.0f / kv_scale : 1.0f;  // IEEE fp32 division, once
+  const float inv_scale = f8 ? 1.0f / kv_scale : 1.0f;  // IEEE fp32 division, once per call
   const uint4* src = static_cast<const uint4*>(rows);
   uint8_t* dst = static_cast<uint8_t*>(kv_cache);
   if (f8)
     mla::mla_kv_pack_kernel<true><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(
         src, page_table, seq_lens, d->batch, d->num_new, d->num_pages, d->max_pages_per_req, d->page_table_stride,
-        inv_scale, dst, status);
+        inv_scale, kv_scale, dst, status);
   else
     mla::mla_kv_pack_kernel<false><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(
         src, page_table, seq_lens, d->batch, d->num_new, d->num_pages, d->max_pages_per_req, d->page_table_stride,
-        inv_scale, dst, status);
+        inv_scale, kv_scale, dst, status);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

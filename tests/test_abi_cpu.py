@@ -278,3 +278,21 @@ def test_binding_constants_match_the_headers():
     # the device status bits are distinct powers of two
     bits = [v for k, v in vals.items() if k.startswith("MLA_DEV_")]
     assert len(set(bits)) == len(bits) and all(b > 0 and b & (b - 1) == 0 for b in bits)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(max_pages_per_req=1 << 25, page_table_stride=1 << 25),  # token positions of a request overflow int32
+    dict(batch=1 << 12, max_pages_per_req=1 << 20, page_table_stride=1 << 20),  # the schedule's page sums
+])
+def test_int32_overflowing_dims_are_unsupported(lib, bad):
+    d = _dims(**bad)
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), 0) == 0
+    rc = lib.mla_decode(ctypes.byref(d), P, P, P, P, P, d.q_len, 1.0, 1.0, P, P, P, 1 << 30, None)
+    assert rc == -2
+    assert lib.mla_decode_noalloc(ctypes.byref(d), P, P, P, P, P, d.q_len, 1.0, 1.0, P, P, None, None) == -2
+
+
+def test_gather_rows_refuses_batches_beyond_the_grid(lib):
+    d = _dims(batch=65536, num_pages=1 << 20)
+    R = ctypes.c_void_p(1 << 20)
+    assert lib.mla_gather_rows(ctypes.byref(d), P, P, P, R, P, P, None) == -2

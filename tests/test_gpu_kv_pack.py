@@ -129,5 +129,25 @@ def test_kv_pack_full_size_sampled():
         t = int(wl.seq_lens[b]) - n_new + i
         page = int(wl.page_table[b, t // 64])
         got = cache[page, t % 64].cpu().numpy()
-        scaled = oracle.kv_pack.bf16_bits_to_f32(wl.rows_bits[b, i]) * (np.float32(1.0) / np.float32(wl.kv_scale))
-        assert np.array_equal(got, oracle.e4m3_encode(scaled.astype(np.float32))), (b, i)
+        assert np.array_equal(got, oracle.kv_pack.quantise_e4m3(wl.rows_bits[b, i], wl.kv_scale)), (b, i)
+
+
+def test_kv_pack_rounds_the_exact_quotient_near_midpoints():
+    """Values whose quotient x / kv_scale lies within a hair of a midpoint
+    between two e4m3 codes, where multiplying by the fp32 reciprocal of the
+    scale would pick the other code: bit-exact against the oracle (exact
+    division), one call per scale."""
+    from kvpack_cases import distinguishing_cases
+
+    rng = np.random.default_rng(21)
+    for x_bits, kv_scale in distinguishing_cases(6):
+        seq_lens = np.array([3], dtype=np.int32)
+        table = _tables(rng, seq_lens, 2, 1)
+        rows = _edge_rows(rng, 1, 3, kv_scale)
+        rows[0, :, :8] = x_bits
+        rows[0, :, 8:16] = x_bits ^ np.uint16(0x8000)  # the same magnitude, negative
+        cache = rng.integers(0, 250, size=(2, 64, 576)).astype(np.uint8)
+        got, status = _run(rows, table, seq_lens, kv_scale, cache, "fp8_e4m3")
+        ref, ref_status = oracle.kv_pack_ref(rows, table, seq_lens, kv_scale, cache, "fp8_e4m3")
+        assert status == ref_status == 0
+        assert np.array_equal(got, ref), (hex(int(x_bits)), kv_scale)

@@ -609,3 +609,35 @@ def test_property_e4m3_encoder_is_monotone():
         assert np.all(np.abs(v) <= 448)
 
     check()
+
+
+def test_kv_pack_quantises_the_exact_quotient():
+    """The tag page's quantisation article quantises a value as round(value /
+    scale).  On inputs where that exact quotient and the fp32 product with
+    the scale's reciprocal round to different e4m3 codes, the oracle writes
+    the code of the exact quotient (checked with rational arithmetic against
+    torch's e4m3 values), and so tells the two readings apart."""
+    from fractions import Fraction
+
+    from kvpack_cases import bits_to_float, distinguishing_cases, e4m3_values, nearest_code
+
+    pytest.importorskip("torch")
+    mags = e4m3_values()
+    cases = distinguishing_cases(8)
+    for xb, s in cases:
+        x = bits_to_float(xb)
+        for sign_bits in (xb, xb ^ np.uint16(0x8000)):
+            xv = bits_to_float(sign_bits)
+            rows = np.full((1, 1, 576), sign_bits, dtype=np.uint16)
+            table = np.array([[0]], dtype=np.int32)
+            out, status = oracle.kv_pack_ref(rows, table, np.array([1], dtype=np.int32), s,
+                                             np.zeros((1, 64, 576), dtype=np.uint8), "fp8_e4m3")
+            assert status == 0
+            exact = nearest_code(Fraction(xv) / Fraction(s), mags)
+            prod = np.float32(np.float32(xv) * (np.float32(1.0) / np.float32(s)))
+            assert out[0, 0, 0] == exact != nearest_code(Fraction(float(prod)), mags), (x, s)
+    # an exact midpoint (power-of-two scale) goes to the even code both ways
+    rows = np.full((1, 1, 576), np.uint16(0x4008), dtype=np.uint16)  # 2.125 = 2 * 1.0625
+    out, _ = oracle.kv_pack_ref(rows, np.array([[0]], dtype=np.int32), np.array([1], dtype=np.int32), 2.0,
+                                np.zeros((1, 64, 576), dtype=np.uint8), "fp8_e4m3")
+    assert out[0, 0, 0] == 0x38  # 1.0625 lies between 1.0 (0x38, even) and 1.125 (0x39)

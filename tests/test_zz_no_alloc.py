@@ -6,9 +6,9 @@ device memory to its own pool at start-up, or a plug-in that only receives
 buffers from its host.  It keeps its scratch (status words, schedule, split
 partials) in a fixed 16 MiB array inside the library instead of a caller
 workspace.  Two calls in a row, made through the C ABI, must agree with
-mla_decode within the parity tolerance (they may split the keys over fewer
-clusters, so only rounding may differ) and with each other bit for bit, and
-the status word they copy out must be clear.
+mla_decode and with the CPU oracle within the parity tolerance (they may
+split the keys over fewer clusters, so only rounding may differ) and with
+each other bit for bit, and the status word they copy out must be clear.
 
 This file is collected last on purpose and also runs on its own.
 """
@@ -65,6 +65,10 @@ def test_noalloc_matches_mla_decode_twice(lib, lens, H, Q, dtype):
     ref_out = ref.out.float().cpu().numpy()
     ref_lse = ref.lse.cpu().numpy()
 
+    import oracle
+
+    ora_out, ora_lse = oracle.mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len,
+                                             wl.scale, wl.kv_scale, wl.kv_dtype)
     dims = mla.make_dims(db.q_nope, db.kv_cache, db.page_table)
     atol, rtol = TOL[dtype]
     results = []
@@ -79,6 +83,8 @@ def test_noalloc_matches_mla_decode_twice(lib, lens, H, Q, dtype):
         l = lse.cpu().numpy()
         assert np.all(np.abs(o - ref_out) <= atol + rtol * np.abs(ref_out))
         assert np.all(np.abs(l - ref_lse) <= atol + rtol * np.abs(ref_lse))
+        assert np.all(np.abs(o - ora_out) <= atol + rtol * np.abs(ora_out))
+        assert np.all(np.abs(l - ora_lse) <= atol + rtol * np.abs(ora_lse))
         results.append((o, l))
     assert np.array_equal(results[0][0], results[1][0]) and np.array_equal(results[0][1], results[1][1])
 
