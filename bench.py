@@ -3,8 +3,9 @@
 
 One step = one decode of a whole synthetic batch (schedule + split-KV
 attention + log-sum-exp combine) through the C ABI.  Default workload: the
-Kimi-K2-shaped batch (B=64 requests, H=64 heads, q_len=1, 8192 cached tokens
-each, 64-token pages, bf16 latent cache).
+largest batch, FP8 speculative verification (B=256 requests, H=128 heads,
+q_len=2 with a causal mask between the drafts, 4096-16384 cached tokens each,
+64-token pages, e4m3 latent cache with one fp32 scale).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
     python bench.py --impl reference ...   # the CPU float64 oracle instead
@@ -21,7 +22,9 @@ so the path shards by request with no collective: weak scaling).
 
 Timing: W untimed warm-up steps, then K steps, each between two CUDA events
 on the launching stream; between steps the L2 is flushed (512 MiB written,
-then read back).  ``value`` is whole-job throughput with inputs resident in
+then read back).  Without --steps, K is sized so the timed steps take about
+a second.  After everything timed, a soak of back-to-back steps (about 1.5 s,
+untimed) records the SM clock under sustained load (``clocks_soak``).  ``value`` is whole-job throughput with inputs resident in
 HBM; ``e2e`` is the same metric through the public call with host buffers
 (inputs up, out and lse down, pipelined on two copy streams);
 ``roofline`` compares the dominant kernel's algorithmic bytes or FLOPs per
@@ -207,6 +210,66 @@ def cpu_oracle_rate(wl, budget_s: float, max_requests: int | None = None):
                                    "cores": cores}
 
 
+def host_info():
+    """CPU model and the BLAS thread count the oracle's matrix products use."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+
+        blas = [i for i in threadpool_info() if i.get("user_api") == "blas"]
+        if blas:
+            threads = int(blas[0]["num_threads"])
+    except Exception:  # threadpoolctl absent (the Arm box) or a library it cannot query
+        pass
+    if threads is None:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                threads = int(os.environ[var])
+                break
+    if threads is None:
+        threads = len(os.sched_getaffinity(0))  # OpenBLAS' default: one thread per usable core
+    return {"cpu_model": model or "unknown", "blas_threads": threads}
+
+
+def whole_batch_parity(wl, go, gl, tol, chunk=32):
+    """out and lse of every request against the oracle, element by element,
+    |gpu - ref| <= tol + tol * |ref|; the oracle runs `chunk` requests at a
+    time so that host memory stays bounded."""
+    import oracle
+
+    t0 = time.perf_counter()
+    max_o = max_l = 0.0
+    bad = 0
+    for b0 in range(0, wl.batch, chunk):
+        reqs = list(range(b0, min(wl.batch, b0 + chunk)))
+        ro, rl = oracle.mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len,
+                                       wl.scale, wl.kv_scale, wl.kv_dtype, requests=reqs)
+        eo = np.abs(go[reqs] - ro[reqs])
+        el = np.abs(gl[reqs] - rl[reqs])
+        max_o, max_l = max(max_o, float(eo.max())), max(max_l, float(el.max()))
+        bad += int(np.sum(eo > tol + tol * np.abs(ro[reqs]))) + int(np.sum(el > tol + tol * np.abs(rl[reqs])))
+    return {"requests": f"all {wl.batch}", "elements": int(go.size + gl.size), "max_abs_out": max_o,
+            "max_abs_lse": max_l, "tolerance": f"{tol} + {tol} * |ref|", "outside_tol": bad,
+            "within_tol": bad == 0, "oracle_seconds": time.perf_counter() - t0}
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -253,6 +316,7 @@ def run_reference(args):
         secs.append(info["seconds"])
         samples.append(info)
     value = float(np.mean(rates))
+    hi = host_info()
     sample_desc = (f"{samples[0]['requests']} request(s) of the {args.config} batch per step "
                    f"({samples[0]['kv_tokens']} KV tokens), float64 numpy oracle")
     line = {
@@ -270,8 +334,9 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": args.config, **wl.describe()},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": samples[0]["cores"], "kind": "oracle",
-                         "sample": sample_desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": hi["blas_threads"], "kind": "oracle",
+                         "sample": sample_desc, "cpu_model": hi["cpu_model"], "blas_threads": hi["blas_threads"],
+                         "usable_cores": samples[0]["cores"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -307,11 +372,6 @@ def run_ours(args):
     flop_peak = bf16_peak * (2.0 if f8 else 1.0)  # e4m3 tensor rate = 2x bf16 (nominal ratio)
     stream = torch.cuda.current_stream()
     flush = L2Flush(dev)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for evs in ev:  # materialise the event handles
-        for e in evs:
-            e.record(stream)
-    torch.cuda.synchronize()
 
     def step(events=None):
         mla.mla_decode(db.q_nope, db.q_pe, db.kv_cache, db.page_table, db.seq_lens, db.q_len, db.scale,
@@ -326,6 +386,26 @@ def run_ours(args):
             print(json.dumps({"error": "device status during warm-up", **mla.timeout_diagnostics(bufs.workspace)}),
                   file=sys.stderr)
             return 3
+    if args.steps is None:  # about one second of timed steps (flush included)
+        t0 = time.perf_counter()
+        for _ in range(3):
+            flush(1)
+            step()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 3
+        steps = max(20, int(np.ceil(1.0 / per)))
+        if world > 1:  # every rank times the same number of steps
+            import torch.distributed as dist
+
+            t = torch.tensor([steps], dtype=torch.int64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            steps = int(t.item())
+        args.steps = steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for evs in ev:  # materialise the event handles
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
 
     if world > 1:
         torch.distributed.barrier()
@@ -357,6 +437,7 @@ def run_ours(args):
     k0_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     k2_ms = [ev[k][2].elapsed_time(ev[k][3]) for k in range(args.steps)]
     ms, job_tokens = reduce_over_ranks(float(np.mean(step_ms)), kv_tokens, dev)
+    ms_median, _ = reduce_over_ranks(float(np.median(step_ms)), kv_tokens, dev)
     value = job_tokens / (ms * 1e-3)
 
     # end to end through the public API with host buffers: every step copies
@@ -442,21 +523,20 @@ def run_ours(args):
     h_out = h_out[(args.steps - 1) % 2]
     h_lse = h_lse[(args.steps - 1) % 2]
 
-    parity = None  # sampled parity against the oracle on this very batch
-    if rank == 0 and not args.no_parity:
-        import oracle
+    # clocks under sustained load: back-to-back steps (with the L2 flush) for
+    # about 1.5 s, untimed, after everything timed above
+    with ClockSampler(dev.index) as clk_soak:
+        t_end = time.perf_counter() + 1.5
+        while time.perf_counter() < t_end:
+            for _ in range(8):
+                flush(1)
+                step()
+            torch.cuda.synchronize()
+    clocks_soak = clk_soak.summary()
 
-        reqs = [0, wl.batch - 1]
-        ro, rl = oracle.mla_decode_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, wl.q_len,
-                                       wl.scale, wl.kv_scale, wl.kv_dtype, requests=reqs)
-        go = out_to_f64(h_out)
-        gl = h_lse.numpy().astype(np.float64)
-        tol = 4e-2 if f8 else 1e-2
-        eo = np.abs(go[reqs] - ro[reqs])
-        el = np.abs(gl[reqs] - rl[reqs])
-        parity = {"requests": reqs, "max_abs_out": float(eo.max()), "max_abs_lse": float(el.max()),
-                  "within_tol": bool(np.all(eo <= tol + tol * np.abs(ro[reqs])) and
-                                     np.all(el <= tol + tol * np.abs(rl[reqs])))}
+    parity = None  # parity against the oracle on this very batch: every request
+    if rank == 0 and not args.no_parity:
+        parity = whole_batch_parity(wl, out_to_f64(h_out), h_lse.numpy().astype(np.float64), 4e-2 if f8 else 1e-2)
 
     k1 = float(np.mean(k1_ms))
     t_bytes = nbytes / (hbm_peak * 1e9)
@@ -467,6 +547,8 @@ def run_ours(args):
     else:
         achieved, peak, unit_r = flops / (k1 * 1e-3) / 1e12, flop_peak, "TFLOP/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit_r, "frac": achieved / peak,
+                "achieved_gbs": nbytes / (k1 * 1e-3) / 1e9, "achieved_tflops": flops / (k1 * 1e-3) / 1e12,
+                "step_gbs": nbytes / (ms * 1e-3) / 1e9, "step_tflops": flops / (ms * 1e-3) / 1e12,
                 "traffic": profiled_traffic(args.config), "traffic_unit": "bytes per launch (ncu dram read + write)",
                 "peak_source": peak_src + (" (e4m3 = 2x bf16, nominal ratio)" if f8 and bound == "tensor" else ""),
                 "kernel": "mla_decode_kernel", "alg_bytes": nbytes, "alg_flops": flops,
@@ -475,9 +557,11 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, info = cpu_oracle_rate(wl, args.cpu_budget)
-        cpu = {"value": rate, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+        hi = host_info()
+        cpu = {"value": rate, "unit": UNIT, "cores": hi["blas_threads"], "kind": "oracle",
                "sample": f"{info['requests']} request(s), {info['kv_tokens']} KV tokens of the {args.config} "
-                         f"batch, float64 numpy oracle, {info['seconds']:.1f} s"}
+                         f"batch, float64 numpy oracle, {info['seconds']:.1f} s",
+               "cpu_model": hi["cpu_model"], "blas_threads": hi["blas_threads"], "usable_cores": info["cores"]}
     nclusters, csize = mla.mla_decode_launch_shape(mla.make_dims(db.q_nope, db.kv_cache, db.page_table),
                                                    dev.index)
     if rank == 0:
@@ -490,6 +574,7 @@ def run_ours(args):
             "warmup": args.warmup,
             "ms_per_step": ms,
             "us_per_step": ms * 1e3,
+            "us_per_step_median": ms_median * 1e3,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -507,8 +592,9 @@ def run_ours(args):
             # schedule, (e4m3: query scales,) attention, combine
             "gpu_launches": (4 if f8 else 3) * args.steps,
             "clocks": clocks,
+            "clocks_soak": clocks_soak,
             "device_status": status,
-            "parity_sample": parity,
+            "parity": parity,
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line))
@@ -802,7 +888,7 @@ def run_sparse(args):
             "e2e": {"value": job_picked / (e2e_ms * 1e-3), "unit": "picked-KV-tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             # gather, schedule, attention, combine
-            "gpu_launches": 4 * args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
+            "gpu_launches": 5 * args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
         }))
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -987,10 +1073,11 @@ def run_reference_kv_pack(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about one second of decode steps; 20 for the other ops)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=list(W.CONFIG_NAMES), default="kimi")
+    ap.add_argument("--config", choices=list(W.CONFIG_NAMES), default="fp8")
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-step-budget", type=float, default=2.0)
@@ -1000,6 +1087,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps is None and (args.op != "decode" or args.impl == "reference"):
+        args.steps = 20
     if args.op == "kv_pack":
         return run_reference_kv_pack(args) if args.impl == "reference" else run_kv_pack(args)
     if args.op == "cascade":

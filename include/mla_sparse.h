@@ -18,7 +18,9 @@
  * -1 marks an unused entry and is skipped silently; any other entry is
  * skipped and raises MLA_DEV_BAD_INDEX.  A repeated position counts as
  * often as it is listed.  A (b, i) with no valid entry raises
- * MLA_DEV_BAD_INDEX and gets out = 0, lse = 0 (one zero row).
+ * MLA_DEV_BAD_INDEX and gets out = 0 and lse = -inf (the log of an empty
+ * sum: the result under which an empty key set drops out of a log-sum-exp
+ * merge).
  *
  * How it runs: a gather kernel packs the selected rows of every (b, i)
  * (the cache's own bytes, bf16 or e4m3) into pages of the workspace; the

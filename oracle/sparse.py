@@ -13,8 +13,11 @@ Readings where the pages are silent:
   causal visibility of draft i); -1 means unused; any other entry is
   skipped and flagged (BAD_INDEX);
 * a position listed twice counts twice (the list is a multiset);
-* a (request, draft) with no used entry is flagged and gets out = 0 and
-  lse = 0 (the result of one all-zero row).
+* a (request, draft) with no used entry is flagged and gets lse = -inf
+  (the natural log of an empty sum) and out = 0: the value of an empty key
+  set under which it drops out of the log-sum-exp merge of split pieces
+  (the same audit section's split-KV merge), as for a query that sees no
+  key in mla_oracle.attend.
 """
 from __future__ import annotations
 
@@ -51,8 +54,8 @@ def mla_decode_sparse_ref(q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, i
                 rows = decode_cache_rows(raw, kv_dtype, kv_scale)
             else:
                 status |= BAD_INDEX
-                rows = np.zeros((1, D_ROW))
+                rows = np.zeros((0, D_ROW))
             qrows = np.concatenate([bf16_bits_to_f64(q_nope[b, i]), bf16_bits_to_f64(q_pe[b, i])], axis=-1)
-            o, l = attend(qrows, rows, rows.shape[0], scale)
+            o, l = attend(qrows, rows, rows.shape[0], scale)  # no rows: out = 0, lse = -inf
             out[b, i], lse[b, i] = o, l
     return out, lse, status

@@ -3,13 +3,14 @@
 // workspace, then the paged decode runs over them as B * q_len requests of
 // one draft position each.
 //
-// Workspace: [status | packed lengths | packed page table | packed rows |
-// decode workspace].  Packed request b' = b * q_len + i owns pages
+// Workspace: [status | packed lengths | empty flags | packed page table |
+// packed rows | decode workspace].  Packed request b' = b * q_len + i owns pages
 // b' * P .. b' * P + P - 1, P = ceil(topk / 64), and its k-th valid entry is
 // its packed row k.
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cmath>
 #include <cstdint>
 
 #include "mla_decode.h"
@@ -45,7 +46,8 @@ __global__ void __launch_bounds__(kChunkEntries)
                            const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ indices, int q_len,
                            int topk, int num_pages, int max_pages, int pt_stride, int p_per,
                            uint8_t* __restrict__ packed, int32_t* __restrict__ packed_pt,
-                           int32_t* __restrict__ packed_len, int32_t* status) {
+                           int32_t* __restrict__ packed_len, int32_t* __restrict__ packed_empty,
+                           int32_t* status) {
   constexpr int kChunks = kRowBytes / 16;
   constexpr int kPer = (kChunks + 31) / 32;
   __shared__ int warp_cnt[kChunkEntries / 32];
@@ -98,12 +100,15 @@ __global__ void __launch_bounds__(kChunkEntries)
         bq * p_per + p;
   const bool last = chunk == static_cast<int>(gridDim.x) - 1;
   const int total = base + total_chunk;
-  if (last && total == 0) {  // nothing to attend: one zero row
+  if (last && total == 0) {  // nothing to attend: one zero row (out = 0; lse is set afterwards)
     if (threadIdx.x == 0) atomicOr(status, MLA_DEV_BAD_INDEX);
     uint4* dst = reinterpret_cast<uint4*>(packed + row0 * kRowBytes);
     for (int c = threadIdx.x; c < kChunks; c += kChunkEntries) dst[c] = make_uint4(0, 0, 0, 0);
   }
-  if (last && threadIdx.x == 0) packed_len[bq] = total > 0 ? total : 1;
+  if (last && threadIdx.x == 0) {
+    packed_len[bq] = total > 0 ? total : 1;
+    packed_empty[bq] = total == 0 ? 1 : 0;
+  }
   __syncwarp();
 
   // copy this warp's rows, kRowsInFlight at a time
@@ -140,12 +145,22 @@ __global__ void __launch_bounds__(kChunkEntries)
   }
 }
 
+// A (b, i) whose list held no valid entry was decoded over one all-zero
+// key, which leaves out = 0 exactly; its lse becomes that of an empty key
+// set, -inf.  One warp per packed request.
+__global__ void __launch_bounds__(256) mla_topk_empty_kernel(const int32_t* __restrict__ packed_empty, int bq_total,
+                                                             int H, float* __restrict__ lse) {
+  const int bq = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (bq >= bq_total || !packed_empty[bq]) return;
+  for (int h = threadIdx.x & 31; h < H; h += 32) lse[static_cast<int64_t>(bq) * H + h] = -INFINITY;
+}
+
 }  // namespace mla
 
 namespace {
 
 struct SparseLayout {
-  size_t status, plen, ppt, rows, dec, total;
+  size_t status, plen, pempty, ppt, rows, dec, total;
 };
 
 bool packed_dims(const mla_dims* d, int32_t topk, mla_dims* pd) {
@@ -170,7 +185,8 @@ bool sparse_layout(const mla_dims* d, int32_t topk, int device, SparseLayout* l,
   const size_t row_bytes = d->kv_dtype == MLA_KV_FP8_E4M3 ? 576 : 1152;
   l->status = 0;
   l->plen = 256;
-  l->ppt = align_up(l->plen + static_cast<size_t>(pd->batch) * 4, 256);
+  l->pempty = align_up(l->plen + static_cast<size_t>(pd->batch) * 4, 256);
+  l->ppt = align_up(l->pempty + static_cast<size_t>(pd->batch) * 4, 256);
   l->rows = align_up(l->ppt + static_cast<size_t>(pd->num_pages) * 4, 1024);
   l->dec = align_up(l->rows + static_cast<size_t>(pd->num_pages) * kPageRows * row_bytes, 256);
   l->total = l->dec + dec;
@@ -219,6 +235,7 @@ int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, c
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws + l.status);
   int32_t* plen = reinterpret_cast<int32_t*>(ws + l.plen);
+  int32_t* pempty = reinterpret_cast<int32_t*>(ws + l.pempty);
   int32_t* ppt = reinterpret_cast<int32_t*>(ws + l.ppt);
   uint8_t* rows = ws + l.rows;
   if (cudaMemsetAsync(status, 0, 4, stream) != cudaSuccess) return MLA_ERR_CUDA;
@@ -227,16 +244,19 @@ int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, c
   if (d->kv_dtype == MLA_KV_FP8_E4M3)
     mla::mla_topk_gather_kernel<576><<<grid, kChunkEntries, 0, stream>>>(
         cache, page_table, seq_lens, indices, d->q_len, topk, d->num_pages, d->max_pages_per_req,
-        d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, status);
+        d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, pempty, status);
   else
     mla::mla_topk_gather_kernel<1152><<<grid, kChunkEntries, 0, stream>>>(
         cache, page_table, seq_lens, indices, d->q_len, topk, d->num_pages, d->max_pages_per_req,
-        d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, status);
+        d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, pempty, status);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
   // the packed problem: request b * q_len + i has one draft position; its
   // queries and outputs are those of (b, i), already laid out that way
-  return mla_decode(&pd, q_nope, q_pe, rows, ppt, plen, 1, scale, kv_scale, out, lse, ws + l.dec,
-                    workspace_bytes - l.dec, stream_v);
+  const int rc = mla_decode(&pd, q_nope, q_pe, rows, ppt, plen, 1, scale, kv_scale, out, lse, ws + l.dec,
+                            workspace_bytes - l.dec, stream_v);
+  if (rc != MLA_OK) return rc;
+  mla::mla_topk_empty_kernel<<<(pd.batch + 7) / 8, 256, 0, stream>>>(pempty, pd.batch, d->num_heads, lse);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int mla_decode_sparse_query_status(const mla_dims* d, int32_t topk, const void* workspace, void* stream_v,

@@ -56,3 +56,16 @@ def compare(wl, out, lse, requests=None, label="", tol=None):
         raise AssertionError(f"{label}: {int(bad_o.sum())} out / {int(bad_l.sum())} lse elements outside "
                              f"tolerance; first out idx {idx}; stats {stats}")
     return stats
+
+
+def compare_chunked(wl, out, lse, label="", tol=None, chunk=32):
+    """compare() over every request of the batch, `chunk` requests at a time;
+    returns the worst error statistics."""
+    worst = {}
+    for b0 in range(0, wl.batch, chunk):
+        reqs = list(range(b0, min(wl.batch, b0 + chunk)))
+        st = compare(wl, out, lse, requests=reqs, label=f"{label} requests {reqs[0]}..{reqs[-1]}", tol=tol)
+        for k, v in st.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    worst["requests"] = wl.batch
+    return worst

@@ -1,7 +1,8 @@
 """The named decode batches at full size, in the launch configuration the
-benchmark times, checked against the oracle on sampled requests (the first,
-the last and the longest) element by element, plus whole-batch properties
-(finite outputs, status word clear)."""
+benchmark times, checked against the oracle element by element on every
+request of the batch (out and lse), plus whole-batch properties (finite
+outputs, status word clear).  The oracle runs request by request in chunks,
+so that host memory stays bounded (the e4m3 batch holds 33.5 M outputs)."""
 import numpy as np
 import pytest
 
@@ -22,15 +23,14 @@ def _lib():
     mla.load_library()
 
 
-from gpu_helpers import compare, run_gpu  # noqa: E402
+from gpu_helpers import compare_chunked, run_gpu  # noqa: E402
 
 
 @pytest.mark.parametrize("name", ["kimi", "dsv3", "prefix", "fp8", "verify4"])
-def test_full_size_config_sampled(name):
+def test_full_size_config_every_request(name):
     wl = W.make_config(name)
     out, lse, status, *_ = run_gpu(wl)
     assert status == 0
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
-    reqs = sorted({0, wl.batch - 1, int(np.argmax(wl.seq_lens))})
-    stats = compare(wl, out, lse, requests=reqs, label=name)
-    print(name, reqs, stats)
+    stats = compare_chunked(wl, out, lse, label=name)
+    print(name, stats)

@@ -84,14 +84,21 @@ def test_sparse_repeated_and_invalid_picks():
     assert check(wl, idx, out, lse) == oracle.sparse.BAD_INDEX
 
 
-def test_sparse_empty_pick_list_gives_zero_row():
-    wl = W.custom([100, 100], num_heads=16, q_len=1, seed=78)
+def test_sparse_empty_pick_list_gives_empty_result():
+    wl = W.custom([100, 100, 300], num_heads=16, q_len=2, seed=78)
     idx = W.topk_indices(wl, 8, seed=6)
     idx[1, 0, :] = -1
+    idx[2, 1, :] = -1
     out, lse, st = run_sparse(wl, idx)
     assert st == oracle.sparse.BAD_INDEX
-    assert np.all(out[1] == 0) and np.all(lse[1] == 0)
+    assert np.all(out[1, 0] == 0) and np.all(lse[1, 0] == -np.inf)
+    assert np.all(out[2, 1] == 0) and np.all(lse[2, 1] == -np.inf)
+    assert np.all(np.isfinite(lse[1, 1])) and np.all(np.isfinite(lse[2, 0]))
     check(wl, idx, out, lse, requests=[0])
+    ro, rl, _ = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, idx,
+                                             wl.scale, requests=[1, 2])
+    assert np.all(np.abs(out[1, 1] - ro[1, 1]) <= 1e-2 + 1e-2 * np.abs(ro[1, 1]))
+    assert np.all(np.abs(lse[2, 0] - rl[2, 0]) <= 1e-2 + 1e-2 * np.abs(rl[2, 0]))
 
 
 def test_sparse_full_size_sampled():

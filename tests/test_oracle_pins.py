@@ -514,7 +514,12 @@ def test_sparse_bad_entries_are_flagged_and_skipped():
     empty = np.full((wl.batch, 2, 3), -1, dtype=np.int32)
     o, l, st = oracle.mla_decode_sparse_ref(wl.q_nope, wl.q_pe, wl.kv_cache, wl.page_table, wl.seq_lens, 2, empty,
                                             wl.scale, requests=[1])
-    assert st == oracle.sparse.BAD_INDEX and np.all(o[1] == 0) and np.all(l[1] == 0)
+    assert st == oracle.sparse.BAD_INDEX and np.all(o[1] == 0) and np.all(l[1] == -np.inf)
+    # merged with any piece by log-sum-exp, the empty list's result is neutral
+    rng = np.random.default_rng(4)
+    po, pl = rng.standard_normal(o[1].shape), rng.standard_normal(l[1].shape)
+    mo, ml = oracle.lse_merge(np.stack([o[1], po]), np.stack([l[1], pl]))
+    assert np.array_equal(mo, po) and np.array_equal(ml, pl)
 
 
 # ------------------------------------------------- properties (hypothesis)
