@@ -29,42 +29,53 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const uint4* p) {
   return v;
 }
 
-// e4m3 code nearest to x / scale when x * inv_scale * (1 - 2^-20) rounds to
-// code ca and x * inv_scale * (1 + 2^-20) to code cb != ca: the two codes are
-// neighbours and the quotient lies on one side of their midpoint m, or on
-// it.  x - m * scale has the sign of (x / scale - m) for scale > 0, and one
-// fma gives that sign exactly (one rounding never changes a sign; only an
-// exact zero is zero).  A tie goes to the even code (mantissa bit 0 clear).
-__device__ __noinline__ uint32_t e4m3_resolve(uint32_t ca, uint32_t cb, float x, float scale) {
-  const float va = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(ca), __NV_E4M3)));
-  const float vb = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(cb), __NV_E4M3)));
-  const float m = 0.5f * (va + vb);  // exact: neighbouring e4m3 values have at most 5 significant bits together
+// Rounding x / scale to e4m3 without a division.  q = x * r, r = fp32(1 /
+// scale), is within 2^-23 (relative) of x / scale, so both round to the same
+// code unless an e4m3 midpoint lies within that distance of q.  Midpoints
+// of e4m3's normal range (2^-6 .. 448: 3 mantissa bits) are the fp32
+// numbers whose mantissa bits 19..0 are 0x80000; q is near one when those
+// bits are within 8 units of it (2^-23 relative is at most 2 units).  Below
+// 2^-6 (the subnormal grid of step 2^-9, midpoints at odd multiples of
+// 2^-10) every value takes the exact path.
+__device__ __forceinline__ bool near_midpoint(float q) {
+  const uint32_t b = __float_as_uint(q);
+  if ((b & 0x7FFFFFFFu) < 0x3C800000u) return true;  // |q| < 2^-6, zero included
+  return ((b & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
+}
+
+// The code nearest to x / scale for a q flagged by near_midpoint: m is the
+// midpoint nearest q (the only one that x / scale can lie across), and
+// x - m * scale, formed by one fma, has exactly the sign of x / scale - m
+// for scale > 0 (one rounding never changes a sign; only an exact zero is
+// zero).  A value just past m on that side (or m itself on a tie, which
+// the conversion sends to the even code) is then converted.
+__device__ __noinline__ uint32_t e4m3_exact(float x, float q, float scale) {
+  float m;
+  if ((__float_as_uint(q) & 0x7FFFFFFFu) < 0x3C800000u) {
+    const float y = fabsf(q) * 1024.f;             // exact: a power of two
+    const float o = 2.f * floorf(0.5f * y) + 1.f;  // the odd integer nearest y
+    m = copysignf(o * 0x1p-10f, q);
+  } else {
+    m = __uint_as_float((__float_as_uint(q) & ~0xFFFFFu) | 0x80000u);
+  }
   const float t = __fmaf_rn(-m, scale, x);
-  if (t > 0.f) return va > vb ? ca : cb;
-  if (t < 0.f) return va > vb ? cb : ca;
-  return (ca & 1u) ? cb : ca;
+  const float v = t > 0.f ? m + fabsf(m) * 0x1p-10f : (t < 0.f ? m - fabsf(m) * 0x1p-10f : m);
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
 
 // e4m3 codes of two bf16 values (packed as in memory, the lower address in
-// the low half) divided by kv_scale: the nearest code to the exact quotient
-// x / kv_scale, ties to even, saturated to +-448.  The quotient is
-// bracketed without a division: with r = fp32(1 / kv_scale), x * r is
-// within 2^-23 (relative) of x / kv_scale, so x * r * (1 -+ 2^-20) lie on
-// either side of it; when both round to the same code, so does the
-// quotient (rounding is monotone), and otherwise (a midpoint within about
-// 2^-20 of the quotient: rare) e4m3_resolve decides.
+// the low half) divided by kv_scale: the code nearest to the exact quotient,
+// ties to even, saturated to +-448.
 __device__ __forceinline__ uint32_t e4m3x2(uint32_t bf2, float inv_scale, float scale) {
   const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bf2));
   const float q0 = __fmul_rn(x.x, inv_scale), q1 = __fmul_rn(x.y, inv_scale);
-  constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
-  const uint32_t lo = static_cast<uint32_t>(
-      __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(q0, kDown), __fmul_rn(q1, kDown)), __NV_SATFINITE, __NV_E4M3));
-  const uint32_t hi = static_cast<uint32_t>(
-      __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(q0, kUp), __fmul_rn(q1, kUp)), __NV_SATFINITE, __NV_E4M3));
-  if (lo == hi) return lo;
-  const uint32_t c0 = (lo & 0xFFu) == (hi & 0xFFu) ? (lo & 0xFFu) : e4m3_resolve(lo & 0xFFu, hi & 0xFFu, x.x, scale);
-  const uint32_t c1 = (lo >> 8) == (hi >> 8) ? (lo >> 8) : e4m3_resolve(lo >> 8, hi >> 8, x.y, scale);
-  return c0 | (c1 << 8);
+  uint32_t c = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3));
+  const bool n0 = near_midpoint(q0), n1 = near_midpoint(q1);
+  if (n0 | n1) {
+    if (n0) c = (c & 0xFF00u) | e4m3_exact(x.x, q0, scale);
+    if (n1) c = (c & 0x00FFu) | (e4m3_exact(x.y, q1, scale) << 8);
+  }
+  return c;
 }
 
 }  // namespace
