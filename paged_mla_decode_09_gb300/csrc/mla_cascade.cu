@@ -4,8 +4,10 @@
 // called with rearranged dimensions on the caller's buffers.
 //
 // Workspace: [status | prefix lengths [B] | suffix lengths [B] | prefix out
-// (bf16 [B][q_len][H][512]) | prefix lse (fp32 [B][q_len][H]) | decode
-// workspace (shared by the passes, which run in order on one stream)].
+// (fp32 [B][q_len][H][512]) | prefix lse (fp32 [B][q_len][H]) | suffix out
+// (fp32, same shape) | decode workspace (shared by the passes, which run in
+// order on one stream)].  Both passes write fp32 results, so that the only
+// rounding to bf16 is the merged output's, as in the plain decode's combine.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -15,6 +17,7 @@
 
 #include "mla_cascade.h"
 #include "mla_decode.h"
+#include "mla_internal.h"
 
 namespace {
 
@@ -53,10 +56,11 @@ __global__ void mla_cascade_or_status_kernel(const int32_t* __restrict__ pass_st
 }
 
 // one warp per query row: out = (e^lp op + e^ls os) / (e^lp + e^ls),
-// lse = ln(e^lp + e^ls); the suffix result is in out / lse and is replaced
+// lse = ln(e^lp + e^ls), from the two passes' fp32 results; the suffix lse
+// is in lse and is replaced
 __global__ void __launch_bounds__(256)
-    mla_cascade_merge_kernel(const __nv_bfloat16* __restrict__ out_pre, const float* __restrict__ lse_pre,
-                             __nv_bfloat16* out, float* lse, int64_t rows) {
+    mla_cascade_merge_kernel(const float* __restrict__ out_pre, const float* __restrict__ lse_pre,
+                             const float* __restrict__ out_suf, __nv_bfloat16* out, float* lse, int64_t rows) {
   const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -66,23 +70,17 @@ __global__ void __launch_bounds__(256)
   const float ws = (ls == -INFINITY) ? 0.f : __expf(ls - m);
   const float z = wp + ws;
   const float ap = z > 0.f ? wp / z : 0.f, as = z > 0.f ? ws / z : 0.f;
-  // 16 values per lane: two 16-byte chunks
-  const uint4* src_p = reinterpret_cast<const uint4*>(out_pre + r * kDL);
-  uint4* dst = reinterpret_cast<uint4*>(out + r * kDL);
+  // 16 values per lane: four float4 of each pass, two 16-byte bf16 chunks out
+  const float4* src_p = reinterpret_cast<const float4*>(out_pre + r * kDL);
+  const float4* src_s = reinterpret_cast<const float4*>(out_suf + r * kDL);
+  uint2* dst = reinterpret_cast<uint2*>(out + r * kDL);
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < 4; ++k) {
     const int c = lane + 32 * k;
-    const uint4 vp = src_p[c], vs = dst[c];
-    const uint32_t wpv[4] = {vp.x, vp.y, vp.z, vp.w}, wsv[4] = {vs.x, vs.y, vs.z, vs.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wpv[e]));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wsv[e]));
-      __nv_bfloat162 y = __floats2bfloat162_rn(ap * a.x + as * b.x, ap * a.y + as * b.y);
-      o[e] = *reinterpret_cast<uint32_t*>(&y);
-    }
-    dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    const float4 a = src_p[c], b = src_s[c];
+    const __nv_bfloat162 y0 = __floats2bfloat162_rn(ap * a.x + as * b.x, ap * a.y + as * b.y);
+    const __nv_bfloat162 y1 = __floats2bfloat162_rn(ap * a.z + as * b.z, ap * a.w + as * b.w);
+    dst[c] = make_uint2(*reinterpret_cast<const uint32_t*>(&y0), *reinterpret_cast<const uint32_t*>(&y1));
   }
   if (lane == 0) lse[r] = z > 0.f ? m + __logf(z) : -INFINITY;
 }
@@ -95,7 +93,7 @@ struct Plan {
   int g;                                // requests per prefix-pass row block
   int b_main, b_tail;                   // requests in the grouped / ungrouped prefix pass
   mla_dims main, tail, suffix;          // the passes' dimensions
-  size_t status, len_pre, len_suf, out_pre, lse_pre, dec, dec_bytes, total;
+  size_t status, len_pre, len_suf, out_pre, lse_pre, out_suf, dec, dec_bytes, total;
 };
 
 bool make_plan(const mla_dims* d, int32_t prefix_pages, int device, Plan* p) {
@@ -136,8 +134,9 @@ bool make_plan(const mla_dims* d, int32_t prefix_pages, int device, Plan* p) {
   p->len_pre = 256;
   p->len_suf = align_up(p->len_pre + B * 4, 256);
   p->out_pre = align_up(p->len_suf + B * 4, 256);
-  p->lse_pre = align_up(p->out_pre + qrows * kDL * 2, 256);
-  p->dec = align_up(p->lse_pre + qrows * 4, 256);
+  p->lse_pre = align_up(p->out_pre + qrows * kDL * 4, 256);
+  p->out_suf = align_up(p->lse_pre + qrows * 4, 256);
+  p->dec = align_up(p->out_suf + qrows * kDL * 4, 256);
   p->dec_bytes = dec;
   p->total = p->dec + dec;
   return true;
@@ -173,8 +172,9 @@ int mla_decode_cascade(const mla_dims* d, const void* q_nope, const void* q_pe, 
   int32_t* status = reinterpret_cast<int32_t*>(ws + p.status);
   int32_t* len_pre = reinterpret_cast<int32_t*>(ws + p.len_pre);
   int32_t* len_suf = reinterpret_cast<int32_t*>(ws + p.len_suf);
-  uint8_t* out_pre = ws + p.out_pre;
+  float* out_pre = reinterpret_cast<float*>(ws + p.out_pre);
   float* lse_pre = reinterpret_cast<float*>(ws + p.lse_pre);
+  float* out_suf = reinterpret_cast<float*>(ws + p.out_suf);
   uint8_t* dec = ws + p.dec;
   const int32_t* dec_status = reinterpret_cast<const int32_t*>(dec);
   if (cudaMemsetAsync(status, 0, 4, stream) != cudaSuccess) return MLA_ERR_CUDA;
@@ -185,29 +185,29 @@ int mla_decode_cascade(const mla_dims* d, const void* q_nope, const void* q_pe, 
   int rc;
   // 1. prefix pass: every draft sees the whole prefix (q_len folded into heads)
   if (p.b_main > 0) {
-    rc = mla_decode(&p.main, q_nope, q_pe, kv_cache, page_table, len_pre, 1, scale, kv_scale, out_pre, lse_pre, dec,
-                    p.dec_bytes, stream_v);
+    rc = mla_decode_f32_out(&p.main, q_nope, q_pe, kv_cache, page_table, len_pre, 1, scale, kv_scale, out_pre,
+                            lse_pre, dec, p.dec_bytes, stream_v);
     if (rc != MLA_OK) return rc;
     mla::mla_cascade_or_status_kernel<<<1, 1, 0, stream>>>(dec_status, status);
   }
   if (p.b_tail > 0) {
     const size_t r0 = static_cast<size_t>(p.b_main) * row_q;
-    rc = mla_decode(&p.tail, static_cast<const uint8_t*>(q_nope) + r0 * kDL * 2,
-                    static_cast<const uint8_t*>(q_pe) + r0 * 64 * 2, kv_cache,
-                    page_table + static_cast<int64_t>(p.b_main) * d->page_table_stride, len_pre, 1, scale, kv_scale,
-                    out_pre + r0 * kDL * 2, lse_pre + r0, dec, p.dec_bytes, stream_v);
+    rc = mla_decode_f32_out(&p.tail, static_cast<const uint8_t*>(q_nope) + r0 * kDL * 2,
+                            static_cast<const uint8_t*>(q_pe) + r0 * 64 * 2, kv_cache,
+                            page_table + static_cast<int64_t>(p.b_main) * d->page_table_stride, len_pre, 1, scale,
+                            kv_scale, out_pre + r0 * kDL, lse_pre + r0, dec, p.dec_bytes, stream_v);
     if (rc != MLA_OK) return rc;
     mla::mla_cascade_or_status_kernel<<<1, 1, 0, stream>>>(dec_status, status);
   }
-  // 2. suffix pass, into the caller's out / lse
-  rc = mla_decode(&p.suffix, q_nope, q_pe, kv_cache, page_table + prefix_pages, len_suf, d->q_len, scale, kv_scale,
-                  out, lse, dec, p.dec_bytes, stream_v);
+  // 2. suffix pass: fp32 out in the workspace, lse in the caller's lse
+  rc = mla_decode_f32_out(&p.suffix, q_nope, q_pe, kv_cache, page_table + prefix_pages, len_suf, d->q_len, scale,
+                          kv_scale, out_suf, lse, dec, p.dec_bytes, stream_v);
   if (rc != MLA_OK) return rc;
   mla::mla_cascade_or_status_kernel<<<1, 1, 0, stream>>>(dec_status, status);
   // 3. merge
   const int64_t rows = static_cast<int64_t>(d->batch) * row_q;
   mla::mla_cascade_merge_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(out_pre), lse_pre, static_cast<__nv_bfloat16*>(out), lse, rows);
+      out_pre, lse_pre, out_suf, static_cast<__nv_bfloat16*>(out), lse, rows);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "mla_decode.h"
+#include "mla_internal.h"
 #include "mla_kernels.cuh"
 
 namespace {
@@ -246,7 +247,7 @@ int check_call(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
 int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
                 const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
                 void* out, float* lse, uint8_t* ws, size_t ws_bytes, bool shrink_to_fit, int32_t* status_out,
-                void* stream_v, void* const* events) {
+                void* stream_v, void* const* events, bool out_f32 = false) {
   int rc = check_call(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, status_out);
   if (rc != MLA_OK) return rc;
   if (!ws) return MLA_ERR_INVALID_ARG;
@@ -293,6 +294,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.max_pages = d->max_pages_per_req;
   p.pt_stride = d->page_table_stride;
   p.unit_cost = mla::unit_cost_pages(f8, R < mla::kRows ? R : mla::kRows);
+  p.out_f32 = out_f32 ? 1 : 0;
   p.scale = scale;
   p.kv_scale = f8 ? kv_scale : 1.f;
   p.timeout_ns = kTimeoutNs;
@@ -400,6 +402,14 @@ int mla_decode_profiled(const mla_dims* d, const void* q_nope, const void* q_pe,
   if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return MLA_ERR_INVALID_ARG;
   return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse,
                      static_cast<uint8_t*>(workspace), workspace_bytes, false, nullptr, stream, events);
+}
+
+int mla_decode_f32_out(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+                       const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale,
+                       float kv_scale, float* out, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse,
+                     static_cast<uint8_t*>(workspace), workspace_bytes, false, nullptr, stream, nullptr, true);
 }
 
 int mla_query_status(const void* workspace, void* stream_v, int32_t* device_status) {
@@ -563,6 +573,15 @@ extern "C" int mla_trace_set_cluster(int cid) {
 extern "C" int mla_trace_cluster_times(void* host_dst, size_t bytes) {
   if (bytes > sizeof(mla::g_mla_cluster_times)) bytes = sizeof(mla::g_mla_cluster_times);
   return cudaMemcpyFromSymbol(host_dst, mla::g_mla_cluster_times, bytes) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+extern "C" int mla_trace_kernel_times(void* host_dst, int reset) {
+  if (cudaMemcpyFromSymbol(host_dst, mla::g_mla_kernel_times, sizeof(mla::g_mla_kernel_times)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (reset) {
+    unsigned long long init[8] = {0, 0, ~0ull, 0, ~0ull, ~0ull, 0, 0};
+    if (cudaMemcpyToSymbol(mla::g_mla_kernel_times, init, sizeof(init)) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
 }
 extern "C" int mla_trace_copy(void* host_dst, size_t bytes) {
   if (bytes > sizeof(mla::g_mla_trace)) bytes = sizeof(mla::g_mla_trace);

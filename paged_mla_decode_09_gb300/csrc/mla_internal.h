@@ -1,0 +1,20 @@
+// Library-internal entry points shared between the translation units of
+// libmla_decode.so (hidden: not part of the C ABI in include/).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mla_decode.h"
+
+extern "C" {
+
+// mla_decode writing fp32 out [B][q_len][H][512] (32-byte aligned) instead
+// of bf16: the cascade's passes keep their partial results unrounded until
+// their merge.
+__attribute__((visibility("hidden"))) int mla_decode_f32_out(
+    const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache, const int32_t* page_table,
+    const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale, float* out, float* lse, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+}  // extern "C"

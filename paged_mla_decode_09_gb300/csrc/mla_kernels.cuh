@@ -210,6 +210,7 @@ struct Params {
   int32_t B, H, Q, R, G, C;
   int32_t num_pages, max_pages, pt_stride;
   int32_t unit_cost;       // schedule weight of a request piece, in pages
+  int32_t out_f32;         // out is fp32 [B][Q][H][512] instead of bf16 (internal: the cascade's passes)
   float scale, kv_scale;
   uint64_t timeout_ns;
 };
@@ -221,6 +222,10 @@ __device__ uint64_t g_mla_trace[2][16][1024];
 // per cluster: [0] start, [1] S producer done, [2] O epilogue of the last unit done
 __device__ uint64_t g_mla_cluster_times[1024][4];
 __device__ int g_mla_trace_cid;  // the cluster whose events are stamped
+// [0] schedule entry, [1] schedule exit, [2] first combine block entry
+// (after its wait), [3] last combine block exit, [4] first attention CTA
+// entry, [5] first attention CTA past its wait
+__device__ unsigned long long g_mla_kernel_times[8];
 #define MLA_TRACE_POINT(role, ev, j)                                                                     \
   do {                                                                                                   \
     if (cluster_id_x() == static_cast<uint32_t>(g_mla_trace_cid) && cluster_ctarank() < 2 && (j) < 1024) \
@@ -254,6 +259,9 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   const bool c_ok = p.C <= kSchedSmemC;
   griddep_launch_dependents();  // the next kernels wait for this one before reading its output
   const int tid = threadIdx.x;
+#ifdef MLA_TRACE
+  if (tid == 0) g_mla_kernel_times[0] = globaltimer_ns();
+#endif
   if (tid == 0) carry = 0;
   __syncthreads();
   for (int base = 0; base < p.B; base += 1024) {
@@ -350,6 +358,10 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     p.rrange[2 * b] = pb1 > pb0 ? clo : 0;
     p.rrange[2 * b + 1] = pb1 > pb0 ? lo : 0;
   }
+#ifdef MLA_TRACE
+  __syncthreads();
+  if (tid == 0) g_mla_kernel_times[1] = globaltimer_ns();
+#endif
 }
 
 // ---------------------------------------------------------------- K0b
@@ -564,7 +576,31 @@ __device__ __forceinline__ void store_row(const Params& p, const Unit& u, int g,
     atomicOr(p.status, MLA_DEV_INTERNAL);
     return;
   }
-  if (u.slot < 0) {
+  if (u.slot < 0 && p.out_f32) {  // unsplit, fp32 output: the values of a partial
+    const int i = rr / p.H, h = rr % p.H;
+    const int64_t orow = (static_cast<int64_t>(u.b) * p.Q + i) * p.H + h;
+    float4* dst = reinterpret_cast<float4*>(p.out + orow * kDL * 4);
+#pragma unroll 1
+    for (int c = half * 256; c < half * 256 + 256; c += 32) {
+      uint32_t v[2][16];
+      tmem_ld16(taddr_row + c, v[0]);
+      tmem_ld16(taddr_row + c + 16, v[1]);
+      tmem_wait_ld_tie(v[0]);
+      tmem_wait_ld_tie(v[1]);
+      if (real) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(v[q][8 * k + e]) * oscale);
+            stg_v8(dst + (c + 16 * q) / 4 + 2 * k, w);  // 8 floats = 32 bytes
+          }
+      }
+    }
+    if (real && half == 0) p.lse[orow] = lse_v;
+  } else if (u.slot < 0) {
     const int i = rr / p.H, h = rr % p.H;
     const int64_t orow = (static_cast<int64_t>(u.b) * p.Q + i) * p.H + h;
     uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kDL * 2);
@@ -750,6 +786,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t partner = rank ^ 1u;
   const int cid = static_cast<int>(cluster_id_x());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[4], globaltimer_ns());
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 6; ++i) {
@@ -800,6 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &ctrl->abort;
 #ifdef MLA_TRACE
   if (threadIdx.x == 0 && rank == 0 && cid < 1024) g_mla_cluster_times[cid][0] = globaltimer_ns();
+  if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[5], globaltimer_ns());
 #endif
 
   if (role_s) {
@@ -1391,6 +1431,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
   griddep_wait();  // the attention kernel's partials (and the schedule) are complete
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[2], globaltimer_ns());
+  struct Exit {  // every warp stamps its exit (warps leave at different points)
+    __device__ ~Exit() {
+      if ((threadIdx.x & 31) == 0) atomicMax(&g_mla_kernel_times[3], globaltimer_ns());
+    }
+  } exit_stamp;
+#endif
   const int b = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.z * 8 + warp;
@@ -1432,6 +1480,13 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
   }
   const int i = rr / p.H, h = rr % p.H;
   const int64_t orow = (static_cast<int64_t>(b) * p.Q + i) * p.H + h;
+  if (p.out_f32) {
+    float4* dstf = reinterpret_cast<float4*>(p.out + orow * kDL * 4);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dstf[lane + 32 * k] = acc[k];
+    if (lane == 0) p.lse[orow] = base + __logf(z);
+    return;
+  }
   uint2* dst = reinterpret_cast<uint2*>(p.out + orow * kDL * 2);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {

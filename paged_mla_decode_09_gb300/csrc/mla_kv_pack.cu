@@ -39,8 +39,7 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const uint4* p) {
 // 2^-10) every value takes the exact path.
 __device__ __forceinline__ bool near_midpoint(float q) {
   const uint32_t b = __float_as_uint(q);
-  if ((b & 0x7FFFFFFFu) < 0x3C800000u) return true;  // |q| < 2^-6, zero included
-  return ((b & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
+  return (b & 0x7FFFFFFFu) < 0x3C800000u || ((b & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
 }
 
 // The code nearest to x / scale for a q flagged by near_midpoint: m is the
@@ -49,7 +48,8 @@ __device__ __forceinline__ bool near_midpoint(float q) {
 // for scale > 0 (one rounding never changes a sign; only an exact zero is
 // zero).  A value just past m on that side (or m itself on a tie, which
 // the conversion sends to the even code) is then converted.
-__device__ __noinline__ uint32_t e4m3_exact(float x, float q, float scale) {
+__device__ __forceinline__ uint32_t e4m3_exact(float x, float scale, float inv_scale) {
+  const float q = __fmul_rn(x, inv_scale);
   float m;
   if ((__float_as_uint(q) & 0x7FFFFFFFu) < 0x3C800000u) {
     const float y = fabsf(q) * 1024.f;             // exact: a power of two
@@ -64,18 +64,14 @@ __device__ __noinline__ uint32_t e4m3_exact(float x, float q, float scale) {
 }
 
 // e4m3 codes of two bf16 values (packed as in memory, the lower address in
-// the low half) divided by kv_scale: the code nearest to the exact quotient,
-// ties to even, saturated to +-448.
-__device__ __forceinline__ uint32_t e4m3x2(uint32_t bf2, float inv_scale, float scale) {
+// the low half) times inv_scale, rounded once; `near` collects, at bits
+// bit0 and bit0 + 1, which of the two quotients e4m3_exact must settle.
+__device__ __forceinline__ uint32_t e4m3x2_fast(uint32_t bf2, float inv_scale, uint32_t& near, int bit0) {
   const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bf2));
   const float q0 = __fmul_rn(x.x, inv_scale), q1 = __fmul_rn(x.y, inv_scale);
-  uint32_t c = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3));
-  const bool n0 = near_midpoint(q0), n1 = near_midpoint(q1);
-  if (n0 | n1) {
-    if (n0) c = (c & 0xFF00u) | e4m3_exact(x.x, q0, scale);
-    if (n1) c = (c & 0x00FFu) | (e4m3_exact(x.y, q1, scale) << 8);
-  }
-  return c;
+  near |= (near_midpoint(q0) ? 1u : 0u) << bit0;
+  near |= (near_midpoint(q1) ? 1u : 0u) << (bit0 + 1);
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3));
 }
 
 }  // namespace
@@ -112,13 +108,29 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int k = 0; k < kPer; ++k)
     if (lane + 32 * k < kChunks) v[k] = ldg_nc_v4(src + lane + 32 * k);
   if constexpr (kF8) {
+    // the code nearest to x / kv_scale: one rounding of x * (1 / kv_scale)
+    // for every value, then the rare values whose quotient lies near a
+    // midpoint between two codes are settled exactly and rewritten
     uint2* dst = reinterpret_cast<uint2*>(cache + slot * kRowVals);  // 8 codes per chunk
+    uint32_t near = 0;  // bit 8k + e: value e of chunk lane + 32k
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       if (lane + 32 * k >= kChunks) break;
-      const uint32_t lo = e4m3x2(v[k].x, inv_scale, scale) | (e4m3x2(v[k].y, inv_scale, scale) << 16);
-      const uint32_t hi = e4m3x2(v[k].z, inv_scale, scale) | (e4m3x2(v[k].w, inv_scale, scale) << 16);
+      const uint32_t lo = e4m3x2_fast(v[k].x, inv_scale, near, 8 * k) |
+                          (e4m3x2_fast(v[k].y, inv_scale, near, 8 * k + 2) << 16);
+      const uint32_t hi = e4m3x2_fast(v[k].z, inv_scale, near, 8 * k + 4) |
+                          (e4m3x2_fast(v[k].w, inv_scale, near, 8 * k + 6) << 16);
       dst[lane + 32 * k] = make_uint2(lo, hi);
+    }
+    if (__any_sync(0xffffffffu, near != 0u)) {
+      const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(src);
+      uint8_t* codes = cache + slot * kRowVals;
+      while (near) {
+        const int bit = __ffs(near) - 1;
+        near &= near - 1u;
+        const int idx = 8 * (lane + 32 * (bit >> 3)) + (bit & 7);  // value index in the row
+        codes[idx] = static_cast<uint8_t>(e4m3_exact(__bfloat162float(xs[idx]), scale, inv_scale));
+      }
     }
   } else {
     uint4* dst = reinterpret_cast<uint4*>(cache + slot * kRowVals * 2);
