@@ -37,11 +37,12 @@ cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, cudaStrea
 }
 
 // Workspace: [status words | page prefix sums | cluster slices | each
-// request's first and last cluster | fp32 partial outputs | partial
-// log-sum-exps | e4m3 query scales].  Sized by B, the cluster count and the
-// number of row blocks only.
+// request's first and last cluster | each request's pieces and their
+// partial slots | the requests cut into pieces | fp32 partial outputs |
+// partial log-sum-exps | e4m3 query scales].  Sized by B, the cluster count
+// and the number of row blocks only.
 struct Layout {
-  size_t status, prefix, cinfo, rrange, o_part, lse_part, qscale, total;
+  size_t status, prefix, cinfo, rrange, pieces, splits, o_part, lse_part, qscale, total;
 };
 
 Layout workspace_layout(int B, int C, int G) {
@@ -50,7 +51,9 @@ Layout workspace_layout(int B, int C, int G) {
   l.prefix = 256;
   l.cinfo = l.prefix + align256(static_cast<size_t>(B + 1) * 4);
   l.rrange = l.cinfo + align256(static_cast<size_t>(C) * 3 * 4);
-  l.o_part = l.rrange + align256(static_cast<size_t>(B) * 2 * 4);
+  l.pieces = l.rrange + align256(static_cast<size_t>(B) * 2 * 4);
+  l.splits = l.pieces + align256(static_cast<size_t>(B) * 8 * 4);
+  l.o_part = l.splits + align256(static_cast<size_t>(1 + (B < C ? B : C)) * 4);
   l.lse_part = l.o_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * mla::kDL * 4);
   l.qscale = l.lse_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * 4);
   l.total = l.qscale + align256(static_cast<size_t>(B) * G * mla::kRows * 4);  // e4m3 query scales
@@ -283,6 +286,8 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
   p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
   p.rrange = reinterpret_cast<int32_t*>(ws + lay.rrange);
+  p.pieces = reinterpret_cast<int32_t*>(ws + lay.pieces);
+  p.splits = reinterpret_cast<int32_t*>(ws + lay.splits);
   p.qscale = reinterpret_cast<float*>(ws + lay.qscale);
   p.B = d->batch;
   p.H = d->num_heads;
@@ -339,7 +344,10 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
     return MLA_ERR_CUDA;
   }
   if (!mark(2)) return MLA_ERR_CUDA;
-  if (launch_pdl(mla::mla_combine_kernel, dim3(d->batch, G, mla::kRows / 8), dim3(256), stream, p) != cudaSuccess) {
+  // one block column per request that may be cut into pieces: at most one
+  // per cluster boundary
+  const unsigned nsplit_max = static_cast<unsigned>(d->batch < C ? d->batch : C);
+  if (launch_pdl(mla::mla_combine_kernel, dim3(nsplit_max, G, mla::kRows / 8), dim3(256), stream, p) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
   }

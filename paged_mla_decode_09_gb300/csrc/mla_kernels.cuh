@@ -206,6 +206,8 @@ struct Params {
   int32_t* prefix;         // [B+1] page prefix sums
   int32_t* cinfo;          // [C][3] = slice start, slice end, first request
   int32_t* rrange;         // [B][2] = first and last cluster whose slice meets the request
+  int32_t* pieces;         // [B][8] = number of pieces, then the partial slots of the first 7 in order
+  int32_t* splits;         // [1 + min(B, C)] = count, then the requests cut into pieces (any order)
   float* qscale;           // [B * R] e4m3 query scales (e4m3 cache only)
   int32_t B, H, Q, R, G, C;
   int32_t num_pages, max_pages, pt_stride;
@@ -254,7 +256,8 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   // global memory is a chain of dependent loads); larger batches read the
   // global arrays
   __shared__ int32_t sp[kSchedSmemB + 1];
-  __shared__ int32_t cs[kSchedSmemC], ce[kSchedSmemC];
+  __shared__ int32_t cs[kSchedSmemC], ce[kSchedSmemC], cf[kSchedSmemC];
+  __shared__ int32_t nsplit;
   const bool sp_ok = p.B <= kSchedSmemB;
   const bool c_ok = p.C <= kSchedSmemC;
   griddep_launch_dependents();  // the next kernels wait for this one before reading its output
@@ -262,7 +265,10 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
 #ifdef MLA_TRACE
   if (tid == 0) g_mla_kernel_times[0] = globaltimer_ns();
 #endif
-  if (tid == 0) carry = 0;
+  if (tid == 0) {
+    carry = 0;
+    nsplit = 0;
+  }
   __syncthreads();
   for (int base = 0; base < p.B; base += 1024) {
     const int b = base + tid;
@@ -334,6 +340,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     if (c_ok) {
       cs[c] = s;
       ce[c] = e;
+      cf[c] = lo;
     }
   }
   __syncthreads();
@@ -357,7 +364,28 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     }
     p.rrange[2 * b] = pb1 > pb0 ? clo : 0;
     p.rrange[2 * b + 1] = pb1 > pb0 ? lo : 0;
+    // the request's pieces in cluster order (empty slices hold none) and
+    // their partial slots: 2c for the piece that starts cluster c's slice,
+    // 2c + 1 for a later one; the combine reads these directly
+    int n = 0;
+    int32_t rec[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (pb1 > pb0 && lo > clo) {
+      for (int c = clo; c <= lo; ++c) {
+        const int s = c_ok ? cs[c] : p.cinfo[3 * c], e = c_ok ? ce[c] : p.cinfo[3 * c + 1];
+        if (s == e) continue;
+        const int f = c_ok ? cf[c] : p.cinfo[3 * c + 2];
+        if (n < 7) rec[1 + n] = 2 * c + (b != f ? 1 : 0);
+        ++n;
+      }
+    }
+    rec[0] = n;
+    int4* dst = reinterpret_cast<int4*>(p.pieces + 8 * static_cast<int64_t>(b));
+    dst[0] = make_int4(rec[0], rec[1], rec[2], rec[3]);
+    dst[1] = make_int4(rec[4], rec[5], rec[6], rec[7]);
+    if (n > 1) p.splits[1 + atomicAdd(&nsplit, 1)] = b;  // at most min(B, C - 1) requests
   }
+  __syncthreads();
+  if (tid == 0) p.splits[0] = nsplit;
 #ifdef MLA_TRACE
   __syncthreads();
   if (tid == 0) g_mla_kernel_times[1] = globaltimer_ns();
@@ -1140,7 +1168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               if (real) {
                 st_async_v4(prow + c * C::kPLbo, make_uint4(wh[0], wh[1], wh[2], wh[3]), bar);
-                st_async_v4(prow + C::kPTermBytes + c * C::kPLbo, make_uint4(wl[0], wl[1], wl[2], wl[3]), bar);
+                if constexpr (C::kPTerms > 1)
+                  st_async_v4(prow + C::kPTermBytes + c * C::kPLbo, make_uint4(wl[0], wl[1], wl[2], wl[3]), bar);
               }
             }
           }
@@ -1439,43 +1468,84 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
     }
   } exit_stamp;
 #endif
-  const int b = blockIdx.x, g = blockIdx.y;
+  // block x: the x-th request cut into pieces (the schedule's list), row
+  // block y, rows 8z .. 8z + 7 (one warp each)
+  if (static_cast<int>(blockIdx.x) >= p.splits[0]) return;
+  const int b = p.splits[1 + blockIdx.x], g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.z * 8 + warp;
   const int rr = g * kRows + r;
   if (rr >= p.R) return;
-  // the clusters whose slice meets the request (from the schedule)
-  const int clo = p.rrange[2 * b], chi = p.rrange[2 * b + 1];
-  if (clo >= chi) return;  // the whole request in one slice (or none): written directly
-  // slices strictly between clo and chi may be empty (fewer pages than
-  // clusters): an empty slice holds no piece and is skipped
-  float mx = -INFINITY;
-  for (int c = clo; c <= chi; ++c) {
-    if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
-    const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
-    mx = fmaxf(mx, p.lse_part[(static_cast<int64_t>(slot) * p.G + g) * kRows + r]);
-  }
-  const float base = (mx == -INFINITY) ? 0.f : mx;
-  float z = 0.f;
-  for (int c = clo; c <= chi; ++c) {
-    if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
-    const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
-    z += __expf(p.lse_part[(static_cast<int64_t>(slot) * p.G + g) * kRows + r] - base);
-  }
+  uint32_t rec[8];
+  ldg_v8(p.pieces + 8 * static_cast<int64_t>(b), rec);
+  const int n = static_cast<int>(rec[0]);
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = clo; c <= chi; ++c) {
-    if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
-    const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
-    const int64_t prow = (static_cast<int64_t>(slot) * p.G + g) * kRows + r;
-    const float w = __expf(p.lse_part[prow] - base) / z;
-    if (w == 0.f) continue;
-    const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * kDL);
+  float base, z;
+  if (n <= 4) {
+    // every piece's lse and partial row in flight at once
+    float ls[4];
+    float4 ov[4][4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float4 v = src[lane + 32 * k];
-      acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
+      ls[k] = -INFINITY;
+      if (k < n) {
+        const int64_t prow = (static_cast<int64_t>(rec[1 + k]) * p.G + g) * kRows + r;
+        ls[k] = p.lse_part[prow];
+        const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * kDL);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ov[k][q] = src[lane + 32 * q];
+      }
+    }
+    float mx = fmaxf(fmaxf(ls[0], ls[1]), fmaxf(ls[2], ls[3]));
+    base = (mx == -INFINITY) ? 0.f : mx;
+    float w[4];
+    z = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[k] = k < n ? __expf(ls[k] - base) : 0.f;
+      z += w[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (k >= n || w[k] == 0.f) continue;
+      const float wk = w[k] / z;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[q].x += wk * ov[k][q].x; acc[q].y += wk * ov[k][q].y;
+        acc[q].z += wk * ov[k][q].z; acc[q].w += wk * ov[k][q].w;
+      }
+    }
+  } else {
+    // more pieces (a request spanning many slices): walk the clusters whose
+    // slice meets it; empty slices hold no piece
+    const int clo = p.rrange[2 * b], chi = p.rrange[2 * b + 1];
+    float mx = -INFINITY;
+    for (int c = clo; c <= chi; ++c) {
+      if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
+      const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
+      mx = fmaxf(mx, p.lse_part[(static_cast<int64_t>(slot) * p.G + g) * kRows + r]);
+    }
+    base = (mx == -INFINITY) ? 0.f : mx;
+    z = 0.f;
+    for (int c = clo; c <= chi; ++c) {
+      if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
+      const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
+      z += __expf(p.lse_part[(static_cast<int64_t>(slot) * p.G + g) * kRows + r] - base);
+    }
+    for (int c = clo; c <= chi; ++c) {
+      if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
+      const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
+      const int64_t prow = (static_cast<int64_t>(slot) * p.G + g) * kRows + r;
+      const float w = __expf(p.lse_part[prow] - base) / z;
+      if (w == 0.f) continue;
+      const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * kDL);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = src[lane + 32 * k];
+        acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
+      }
     }
   }
   const int i = rr / p.H, h = rr % p.H;

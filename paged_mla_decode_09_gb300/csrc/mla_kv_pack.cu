@@ -31,47 +31,60 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const uint4* p) {
 
 // Rounding x / scale to e4m3 without a division.  q = x * r, r = fp32(1 /
 // scale), is within 2^-23 (relative) of x / scale, so both round to the same
-// code unless an e4m3 midpoint lies within that distance of q.  Midpoints
-// of e4m3's normal range (2^-6 .. 448: 3 mantissa bits) are the fp32
-// numbers whose mantissa bits 19..0 are 0x80000; q is near one when those
-// bits are within 8 units of it (2^-23 relative is at most 2 units).  Below
-// 2^-6 (the subnormal grid of step 2^-9, midpoints at odd multiples of
-// 2^-10) every value takes the exact path.
-__device__ __forceinline__ bool near_midpoint(float q) {
-  const uint32_t b = __float_as_uint(q);
-  return (b & 0x7FFFFFFFu) < 0x3C800000u || ((b & 0xFFFFFu) - 0x80000u + 8u) <= 16u;
+// code unless an e4m3 midpoint lies within that distance of q.  In e4m3's
+// normal range (2^-6 .. 448: 3 mantissa bits) the midpoints are the fp32
+// numbers whose mantissa bits 19..0 are 0x80000, and q is near one when
+// those bits are within 8 units of it (2^-23 relative is at most 2 units).
+// Nonzero q below 2^-6 (the subnormal grid) are always sent to the exact
+// path; zero converts exactly.
+__device__ __forceinline__ bool needs_exact(float q) {
+  const uint32_t b = __float_as_uint(q) & 0x7FFFFFFFu;
+  return (b - 1u) < 0x3C7FFFFFu || ((b + 8u) & 0xFFFF0u) == 0x80000u;
 }
 
-// The code nearest to x / scale for a q flagged by near_midpoint: m is the
-// midpoint nearest q (the only one that x / scale can lie across), and
-// x - m * scale, formed by one fma, has exactly the sign of x / scale - m
-// for scale > 0 (one rounding never changes a sign; only an exact zero is
-// zero).  A value just past m on that side (or m itself on a tie, which
-// the conversion sends to the even code) is then converted.
-__device__ __forceinline__ uint32_t e4m3_exact(float x, float scale, float inv_scale) {
+// The code nearest to x / scale: m is the midpoint nearest q (the only one
+// that x / scale can lie across), and x - m * scale, formed by one fma, has
+// exactly the sign of x / scale - m for scale > 0 (one rounding never
+// changes a sign; only an exact zero is zero).  A value just past m on that
+// side (or m itself on a tie, which the conversion sends to the even code)
+// is then converted.  The subnormal range [0, 2^-6) has the grid step of the
+// binade [2^-6, 2^-5) (2^-9), so |q| + 2^-6 locates its midpoint there.
+__device__ __noinline__ uint32_t e4m3_exact(float x, float scale, float inv_scale) {
   const float q = __fmul_rn(x, inv_scale);
-  float m;
-  if ((__float_as_uint(q) & 0x7FFFFFFFu) < 0x3C800000u) {
-    const float y = fabsf(q) * 1024.f;             // exact: a power of two
-    const float o = 2.f * floorf(0.5f * y) + 1.f;  // the odd integer nearest y
-    m = copysignf(o * 0x1p-10f, q);
-  } else {
-    m = __uint_as_float((__float_as_uint(q) & ~0xFFFFFu) | 0x80000u);
-  }
+  const float shift = fabsf(q) < 0x1p-6f ? 0x1p-6f : 0.f;
+  // g may round (by at most 2^-30), which can only move it across a code
+  // value, never across a midpoint; the midpoint found on either side of a
+  // code value still lies between x / scale and the code it does not round to
+  const float g = fabsf(q) + shift;
+  const float mi = __uint_as_float((__float_as_uint(g) & ~0xFFFFFu) | 0x80000u);
+  const float m = copysignf(mi - shift, q);
   const float t = __fmaf_rn(-m, scale, x);
   const float v = t > 0.f ? m + fabsf(m) * 0x1p-10f : (t < 0.f ? m - fabsf(m) * 0x1p-10f : m);
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-// e4m3 codes of two bf16 values (packed as in memory, the lower address in
-// the low half) times inv_scale, rounded once; `near` collects, at bits
-// bit0 and bit0 + 1, which of the two quotients e4m3_exact must settle.
-__device__ __forceinline__ uint32_t e4m3x2_fast(uint32_t bf2, float inv_scale, uint32_t& near, int bit0) {
-  const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bf2));
-  const float q0 = __fmul_rn(x.x, inv_scale), q1 = __fmul_rn(x.y, inv_scale);
-  near |= (near_midpoint(q0) ? 1u : 0u) << bit0;
-  near |= (near_midpoint(q1) ? 1u : 0u) << (bit0 + 1);
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3));
+// e4m3 codes of the 8 bf16 values of a 16-byte chunk divided by kv_scale:
+// one rounding of x * (1 / kv_scale) each, then, for a chunk holding a value
+// that needs it (rare), the exact code of every value
+__device__ __forceinline__ uint2 e4m3x8(uint4 v, float inv_scale, float scale) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
+  bool flag = false;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    const float q0 = __fmul_rn(x.x, inv_scale), q1 = __fmul_rn(x.y, inv_scale);
+    flag |= needs_exact(q0) | needs_exact(q1);
+    c[k] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3));
+  }
+  if (flag) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      c[k] = e4m3_exact(x.x, scale, inv_scale) | (e4m3_exact(x.y, scale, inv_scale) << 8);
+    }
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 }  // namespace
@@ -108,30 +121,11 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int k = 0; k < kPer; ++k)
     if (lane + 32 * k < kChunks) v[k] = ldg_nc_v4(src + lane + 32 * k);
   if constexpr (kF8) {
-    // the code nearest to x / kv_scale: one rounding of x * (1 / kv_scale)
-    // for every value, then the rare values whose quotient lies near a
-    // midpoint between two codes are settled exactly and rewritten
+    // the code nearest to x / kv_scale (see e4m3x8)
     uint2* dst = reinterpret_cast<uint2*>(cache + slot * kRowVals);  // 8 codes per chunk
-    uint32_t near = 0;  // bit 8k + e: value e of chunk lane + 32k
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      if (lane + 32 * k >= kChunks) break;
-      const uint32_t lo = e4m3x2_fast(v[k].x, inv_scale, near, 8 * k) |
-                          (e4m3x2_fast(v[k].y, inv_scale, near, 8 * k + 2) << 16);
-      const uint32_t hi = e4m3x2_fast(v[k].z, inv_scale, near, 8 * k + 4) |
-                          (e4m3x2_fast(v[k].w, inv_scale, near, 8 * k + 6) << 16);
-      dst[lane + 32 * k] = make_uint2(lo, hi);
-    }
-    if (__any_sync(0xffffffffu, near != 0u)) {
-      const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(src);
-      uint8_t* codes = cache + slot * kRowVals;
-      while (near) {
-        const int bit = __ffs(near) - 1;
-        near &= near - 1u;
-        const int idx = 8 * (lane + 32 * (bit >> 3)) + (bit & 7);  // value index in the row
-        codes[idx] = static_cast<uint8_t>(e4m3_exact(__bfloat162float(xs[idx]), scale, inv_scale));
-      }
-    }
+    for (int k = 0; k < kPer; ++k)
+      if (lane + 32 * k < kChunks) dst[lane + 32 * k] = e4m3x8(v[k], inv_scale, scale);
   } else {
     uint4* dst = reinterpret_cast<uint4*>(cache + slot * kRowVals * 2);
 #pragma unroll
