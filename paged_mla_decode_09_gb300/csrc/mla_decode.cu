@@ -308,7 +308,6 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   auto mark = [&](int k) {
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[k]), stream) == cudaSuccess;
   };
-  if (cudaMemsetAsync(p.status, 0, 16, stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (!mark(0)) return MLA_ERR_CUDA;
   mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
@@ -567,7 +566,7 @@ extern "C" int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const v
   if ((rc = device_ok(dev)) != MLA_OK) return rc;
   uint8_t* ws = nullptr;
   if ((rc = noalloc_scratch(dev, &ws)) != MLA_OK) return rc;
-  // the status words start at zero (decode_impl clears them); everything
+  // the status words start at zero (the schedule kernel clears them); everything
   // else in the scratch is written before it is read within the call
   return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, ws,
                      kNoAllocScratchBytes, true, status_out, stream, nullptr);
