@@ -1060,11 +1060,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (r == 0) MLA_TRACE_POINT(0, 3, j);
           tc_fence_after();
+          // S of the page, each load with the maximum of its 16 columns
+          // (sm_103a's TMEM load with max-reduction)
           uint32_t v[4][16];
+          float red[4];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tmem + lane_base + kSCol0 + sb * 64 + q4 * 16, v[q4]);
+          for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_max(tmem + lane_base + kSCol0 + sb * 64 + q4 * 16, v[q4], red[q4]);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld_tie(v[q4]);
+          for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld_tie(v[q4], red[q4]);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctrl->s_empty[sb]));
@@ -1073,13 +1076,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // every key of the page visible to the row: no per-key masking
           const bool full = t0 + kPage <= nvis;
 #define MLA_S(t) __uint_as_float(v[(t) >> 4][(t) & 15])
-          // max of the raw scores (c2 > 0, so scaling commutes with max);
-          // unused slots (even NaN) never pass the mask
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (full) {
-#pragma unroll
-            for (int t = 0; t < 64; ++t) m4[t & 3] = fmaxf(m4[t & 3], MLA_S(t));
-          } else {
+          // max of the raw scores (c2 > 0, so scaling commutes with max): on
+          // a full page the loads' reduced values; otherwise masked here, so
+          // that unused slots (even NaN) never count
+          float m4[4] = {red[0], red[1], red[2], red[3]};
+          if (!full) {
+            m4[0] = m4[1] = m4[2] = m4[3] = -INFINITY;
 #pragma unroll
             for (int t = 0; t < 64; ++t)
               if (t0 + t < nvis) m4[t & 3] = fmaxf(m4[t & 3], MLA_S(t));
@@ -1121,27 +1123,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (r == 0) MLA_TRACE_POINT(0, 8, j);
           l *= ex2_approx(m_run - m_ref);  // m_run <= m_ref: the partial sum moves to the new frame
           m_run = m_ref;
-          // P slot ps_slot is free once the O CTA finished PV of page j - ps.n
+          // P (swizzled for the MMA) goes 16 bytes at a time into the O CTA's
+          // shared memory, completing bytes on its p_full barrier, once P
+          // slot ps_slot is free (the O CTA finished PV of page j - ps.n);
+          // then the row's reference.  bf16: P is computed into registers
+          // before the slot is waited for, which takes P's arithmetic off the
+          // slot's round trip (blocks of more than 64 rows have two slots:
+          // measured 5-11 % faster).  e4m3 (three slots, never waited for
+          // long): each chunk is sent as soon as it is computed, so the
+          // stores overlap the arithmetic (measured 1 % faster than the other
+          // order).
           const int ps_slot = static_cast<int>(j % static_cast<uint32_t>(ps.n));
           const uint32_t ps_phase = (j / static_cast<uint32_t>(ps.n)) & 1;
-          if (!mbar_wait_warp<true, true>(smem_u32(&ctrl->p_empty[ps_slot]), ps_phase ^ 1, abort, p.timeout_ns)) {
-            ok = false;
-            why = kWaitPEmptyS;
-            break;
-          }
-          if (r == 0) MLA_TRACE_POINT(0, 4, j);
-          // P (swizzled for the MMA) is computed 16 bytes at a time and each
-          // chunk goes straight into the O CTA's shared memory, completing
-          // bytes on its p_full barrier; then the row's reference
           const float nm = SoftmaxCfg<kF8>::kShift - m_ref;  // P = 2^(s * c2 - m_ref + shift)
-          const uint32_t bar = mapa(smem_u32(&ctrl->p_full[ps_slot]), partner);
-          const uint32_t prow = p_remote + ps_slot * ps.stride + (r >> 3) * C::kPSbo + (r & 7) * 16;
           auto prob = [&](int t) {
             const float e = ex2_approx(fmaf(MLA_S(t), c2, nm));
             return (full || t0 + t < nvis) ? e : 0.f;
           };
+          const uint32_t bar = mapa(smem_u32(&ctrl->p_full[ps_slot]), partner);
+          const uint32_t prow = p_remote + ps_slot * ps.stride + (r >> 3) * C::kPSbo + (r & 7) * 16;
           float s4[4] = {0.f, 0.f, 0.f, 0.f};
           if constexpr (!kF8) {
+            uint4 pw[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {  // keys 8c .. 8c + 7
               uint32_t w[4];
@@ -1152,9 +1155,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
                 w[k] = *reinterpret_cast<uint32_t*>(&b2);
               }
-              if (real) st_async_v4(prow + c * C::kPLbo, make_uint4(w[0], w[1], w[2], w[3]), bar);
+              pw[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (!mbar_wait_warp<true, true>(smem_u32(&ctrl->p_empty[ps_slot]), ps_phase ^ 1, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitPEmptyS;
+              break;
+            }
+            if (r == 0) MLA_TRACE_POINT(0, 4, j);
+            if (real) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) st_async_v4(prow + c * C::kPLbo, pw[c], bar);
             }
           } else {
+            if (!mbar_wait_warp<true, true>(smem_u32(&ctrl->p_empty[ps_slot]), ps_phase ^ 1, abort, p.timeout_ns)) {
+              ok = false;
+              why = kWaitPEmptyS;
+              break;
+            }
+            if (r == 0) MLA_TRACE_POINT(0, 4, j);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {  // keys 16c .. 16c + 15
               uint32_t wh[4], wl[4];

@@ -380,6 +380,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// tmem_ld16 plus the maximum of the 16 loaded fp32 values of this thread's
+// lane (sm_103a's TMEM load with max-reduction; a NaN among them is skipped
+// unless the .NaN form is used).  Valid after tmem_wait_ld_tie on r.
+__device__ __forceinline__ void tmem_ld16_max(uint32_t taddr, uint32_t (&r)[16], float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, %16, [%17];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=f"(mx)
+      : "r"(taddr));
+}
+
 // Waits for this thread's outstanding tcgen05.ld; the registers are tied to
 // the wait so no use of them can be scheduled before it.
 __device__ __forceinline__ void tmem_wait_ld_tie(uint32_t (&r)[16]) {
@@ -387,6 +400,14 @@ __device__ __forceinline__ void tmem_wait_ld_tie(uint32_t (&r)[16]) {
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                  "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
                  "+r"(r[15])::"memory");
+}
+
+// tmem_wait_ld_tie for a tmem_ld16_max: the reduced value is tied too.
+__device__ __forceinline__ void tmem_wait_ld_tie(uint32_t (&r)[16], float& mx) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+f"(mx)::"memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
