@@ -1240,16 +1240,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const PSlots ps(kF8, rows_real);
     if (warp == 0) {
       if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, &tm_qn, &tm_qp, cid, partner);
-    } else if (warp == 3) {
-      // ---- waiter: gets page j ready for PV (c_kv landed, tail rows zeroed,
-      // P arrived, O free and rescaled) while the MMA warp issues PV(j - 1);
-      // the MMA warp then waits on one barrier per page
+    } else if (warp == 1) {
+      // ---- PV warp: for page j it waits until the page is ready for PV
+      // (c_kv landed, P arrived, O free on a unit's first page: the
+      // independent conditions polled together), has O rescaled first when
+      // a row's reference rose, zeroes the tail rows of a request's last
+      // page, and issues PV(j); the whole warp runs the loop and one elected
+      // lane issues.  (A separate waiter warp that prepared page j while
+      // this one issued PV(j - 1) added a second poll between P's arrival
+      // and its PV.)
       UnitIter it;
       it.init(p, cid);
       Unit u;
       uint32_t j = 0, un = 0;
       bool ok = true;
       int why = 0;
+      const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << partner));
       // the S CTA sends the P rows (and O scale factors) of real query rows
       // only, and every softmax warp's flag word
       const uint32_t ptx = static_cast<uint32_t>(rows_real) * C::kPTxRow + C::kPTxFlags;
@@ -1265,26 +1271,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
           const uint32_t pph = (j / static_cast<uint32_t>(ps.n)) & 1;
           uint8_t* slot = ring + st * C::kSlotO;
-          if (lane == 0) MLA_TRACE_POINT(1, 8, j);
           const bool first = pg == u.p0;
-          if (first && !mbar_wait_warp(smem_u32(&ctrl->o_empty), (un & 1) ^ 1, abort, p.timeout_ns)) {
-            ok = false;
-            why = kWaitOEmpty;
-            break;
-          }
-          {  // PV(j - 1) taken, c_kv landed, P arrived
-            const uint32_t bars[4] = {j > 0 ? smem_u32(&ctrl->pv_taken) : 0u, smem_u32(&ctrl->kv_full[st]),
+          if (lane == 0) MLA_TRACE_POINT(1, 8, j);
+          {  // O free (a unit's first page), c_kv landed, P arrived
+            const uint32_t bars[4] = {first ? smem_u32(&ctrl->o_empty) : 0u, smem_u32(&ctrl->kv_full[st]),
                                       smem_u32(&ctrl->p_full[pb]), 0u};
-            const uint32_t pars[4] = {(j - 1) & 1, kph, pph, 0u};
+            const uint32_t pars[4] = {(un & 1) ^ 1, kph, pph, 0u};
             if (!mbar_wait4_warp(bars, pars, abort, p.timeout_ns)) {
               ok = false;
               why = kWaitPFullO;
               break;
             }
           }
+          if (lane == 0) MLA_TRACE_POINT(1, 1, j);
           // a page on which some row's reference rose needs O rescaled first
-          // (after PV(j - 1)): the correction warps do it and acknowledge.
-          // PV(j) waits for that, so one request at most is outstanding.
+          // (after PV(j - 1), the last one issued): the correction warps do it
+          // and acknowledge
           const uint32_t fw = lane < 4 ? flag_buf[pb * 4 + lane] : 0u;
           if (__any_sync(0xffffffffu, fw != 0u)) {
             if (lane == 0) {
@@ -1302,49 +1304,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           // bytes cannot come earlier: the S CTA sends them only after PV(j)
           // ended.
           if (lane == 0) mbar_expect_tx(smem_u32(&ctrl->p_full[pb]), ptx);
-          if (lane == 0) MLA_TRACE_POINT(1, 1, j);
           const int valid = u.L - pg * kPage;
           if (valid < kPage) {
             // token rows past the sequence end may hold anything (even NaN):
             // zero them so that P = 0 there cannot turn into 0 * NaN
             // lane: 16-byte chunk lane % 8 of rows v0 + lane / 8, + 4, ... in
-            // every box (no division: this warp is on the path to PV)
+            // every box (no division on the path to PV)
             const int v0 = valid > 0 ? valid : 0;
             const int chunk = lane & 7;
             for (int rowi = v0 + (lane >> 3); rowi < kPage; rowi += 4)
 #pragma unroll
               for (int box = 0; box < C::kBoxesPartO; ++box)
                 *reinterpret_cast<uint4*>(slot + box * C::kBox + rowi * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-            fence_proxy_async_cta();
             __syncwarp();
           }
-          if (lane == 0) MLA_TRACE_POINT(1, 2, j);
-          if (lane == 0) MLA_TRACE_POINT(1, 9, j);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctrl->pv_ready));
-        }
-        ++un;
-      }
-      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
-    } else if (warp == 1) {
-      // ---- PV issuer
-      UnitIter it;
-      it.init(p, cid);
-      Unit u;
-      uint32_t j = 0;
-      bool ok = true;
-      const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << partner));
-      while (ok && it.next(u)) {
-        for (int pg = u.p0; pg < u.p1; ++pg, ++j) {
-          if (!mbar_wait_warp(smem_u32(&ctrl->pv_ready), j & 1, abort, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) mbar_arrive(smem_u32(&ctrl->pv_taken));
           if (lane == 0) MLA_TRACE_POINT(1, 10, j);
-          const int st = j % C::kNStO;
-          const int pb = static_cast<int>(j % static_cast<uint32_t>(ps.n));
-          const bool first = pg == u.p0;
           fence_proxy_async_cta();
           tc_fence_after();
           {  // the whole warp issues; one elected lane executes
@@ -1368,8 +1342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) MLA_TRACE_POINT(1, 3, j);
           }
         }
+        ++un;
       }
-      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, kWaitPvReady, j);
+      if (!ok && lane == 0) raise_timeout(p, ctrl, partner, why, j);
       mma_commit_e(smem_u32(&ctrl->drain));
       if (lane == 0) {
         const uint64_t t0 = globaltimer_ns();
