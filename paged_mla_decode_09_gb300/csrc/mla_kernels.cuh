@@ -221,7 +221,10 @@ struct Params {
 };
 
 // Optional event trace (built only with -DMLA_TRACE): global-timer stamps
-// of each pipeline event per page for cluster 0, for latency analysis.
+// of each pipeline event per page for one cluster, for latency analysis, and
+// of each cluster's start and end and the kernels' entries and exits.  With
+// -DMLA_TRACE_NO_PAGES as well, only the latter (a few stamps per cluster:
+// timings close to those of the normal build).
 #ifdef MLA_TRACE
 __device__ uint64_t g_mla_trace[2][16][1024];
 // per cluster: [0] start, [1] S producer done, [2] O epilogue of the last unit done
@@ -231,6 +234,8 @@ __device__ int g_mla_trace_cid;  // the cluster whose events are stamped
 // (after its wait), [3] last combine block exit, [4] first attention CTA
 // entry, [5] first attention CTA past its wait
 __device__ unsigned long long g_mla_kernel_times[8];
+#endif
+#if defined(MLA_TRACE) && !defined(MLA_TRACE_NO_PAGES)
 #define MLA_TRACE_POINT(role, ev, j)                                                                     \
   do {                                                                                                   \
     if (cluster_id_x() == static_cast<uint32_t>(g_mla_trace_cid) && cluster_ctarank() < 2 && (j) < 1024) \
@@ -551,10 +556,11 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
   };
   if (have_next) prefetch_q(un_next);
   while (ok && it.next(u)) {
-    if (kRoleS) {
-      have_next = have_next && nxt.next(un_next);
-      if (have_next) prefetch_q(un_next);
-    }
+    // the next unit's query rows are pulled into L2 when this unit has a
+    // few pages left to copy (~10 pages before they are read): issued at the
+    // unit's start, a long unit's page stream evicted them again
+    if (kRoleS) have_next = have_next && nxt.next(un_next);
+    const int pf_page = u.p1 - 4 > u.p0 ? u.p1 - 4 : u.p0;
     for (int e = 0; e < qe && ok; ++e) {
       uint32_t bar;
       uint8_t* slot;
@@ -569,6 +575,7 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
       ++i;
     }
     for (int pg = u.p0; pg < u.p1 && ok; ++pg, ++j) {
+      if (kRoleS && have_next && pg == pf_page) prefetch_q(un_next);
       const int32_t pid = read_page_id(p, u.b, pg);
       const int y = pid * kPage;
       uint32_t bar;
