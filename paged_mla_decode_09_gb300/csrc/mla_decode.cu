@@ -346,7 +346,11 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   // one block column per request that may be cut into pieces: at most one
   // per cluster boundary
   const unsigned nsplit_max = static_cast<unsigned>(d->batch < C ? d->batch : C);
-  if (launch_pdl(mla::mla_combine_kernel, dim3(nsplit_max, G, mla::kRows / 8), dim3(256), stream, p) != cudaSuccess) {
+  // rows per row block that exist (R < 128: only the first R)
+  const unsigned zrows = static_cast<unsigned>(((R < mla::kRows ? R : mla::kRows) + mla::kCombineWarps - 1) /
+                                               mla::kCombineWarps);
+  if (launch_pdl(mla::mla_combine_kernel, dim3(nsplit_max, G, zrows), dim3(mla::kCombineWarps * 32), stream, p) !=
+      cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
   }

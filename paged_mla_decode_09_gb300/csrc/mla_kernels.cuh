@@ -1477,7 +1477,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merges the fp32 partials of every request cut by a slice boundary:
 // lse = log sum_s exp(lse_s), out = sum_s exp(lse_s - lse) * out_s.
 
-__global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
+// 128 threads (4 warps, one query row each) and few registers per thread,
+// so that the whole grid is resident at once when the attention kernel ends
+// (with 256-thread blocks of ~100 registers only two fit per SM, and a Kimi
+// batch's combine ran in three and a half waves).
+constexpr int kCombineWarps = 4;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(Params p) {
   griddep_wait();  // the attention kernel's partials (and the schedule) are complete
 #ifdef MLA_TRACE
   if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[2], globaltimer_ns());
@@ -1488,11 +1494,11 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
   } exit_stamp;
 #endif
   // block x: the x-th request cut into pieces (the schedule's list), row
-  // block y, rows 8z .. 8z + 7 (one warp each)
+  // block y, rows 4z .. 4z + 3 (one warp each)
   if (static_cast<int>(blockIdx.x) >= p.splits[0]) return;
   const int b = p.splits[1 + blockIdx.x], g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.z * 8 + warp;
+  const int r = blockIdx.z * kCombineWarps + warp;
   const int rr = g * kRows + r;
   if (rr >= p.R) return;
   uint32_t rec[8];
@@ -1502,39 +1508,54 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   float base, z;
-  if (n <= 4) {
-    // every piece's lse and partial row in flight at once
-    float ls[4];
-    float4 ov[4][4];
+  auto prow_of = [&](int slot) { return (static_cast<int64_t>(slot) * p.G + g) * kRows + r; };
+  auto add = [&](float w, const float4 (&v)[4]) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      ls[k] = -INFINITY;
-      if (k < n) {
-        const int64_t prow = (static_cast<int64_t>(rec[1 + k]) * p.G + g) * kRows + r;
-        ls[k] = p.lse_part[prow];
-        const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * kDL);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ov[k][q] = src[lane + 32 * q];
-      }
+    for (int q = 0; q < 4; ++q) {
+      acc[q].x += w * v[q].x; acc[q].y += w * v[q].y; acc[q].z += w * v[q].z; acc[q].w += w * v[q].w;
     }
-    float mx = fmaxf(fmaxf(ls[0], ls[1]), fmaxf(ls[2], ls[3]));
+  };
+  if (n == 2) {
+    // the common case: both pieces' lse and partial rows in flight at once
+    const int64_t p0 = prow_of(static_cast<int>(rec[1])), p1 = prow_of(static_cast<int>(rec[2]));
+    const float l0 = p.lse_part[p0], l1 = p.lse_part[p1];
+    float4 v0[4], v1[4];
+    const float4* s0 = reinterpret_cast<const float4*>(p.o_part + p0 * kDL);
+    const float4* s1 = reinterpret_cast<const float4*>(p.o_part + p1 * kDL);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v0[q] = s0[lane + 32 * q];
+      v1[q] = s1[lane + 32 * q];
+    }
+    const float mx = fmaxf(l0, l1);
     base = (mx == -INFINITY) ? 0.f : mx;
-    float w[4];
+    const float w0 = __expf(l0 - base), w1 = __expf(l1 - base);
+    z = w0 + w1;
+    if (w0 != 0.f) add(w0 / z, v0);
+    if (w1 != 0.f) add(w1 / z, v1);
+  } else if (n <= 7) {
+    // the record's slots: all lse first, then the partial rows one by one
+    float ls[7];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 7; ++k) {
+      ls[k] = k < n ? p.lse_part[prow_of(static_cast<int>(rec[1 + k]))] : -INFINITY;
+      mx = fmaxf(mx, ls[k]);
+    }
+    base = (mx == -INFINITY) ? 0.f : mx;
     z = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      w[k] = k < n ? __expf(ls[k] - base) : 0.f;
-      z += w[k];
-    }
+    for (int k = 0; k < 7; ++k) z += k < n ? __expf(ls[k] - base) : 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (k >= n || w[k] == 0.f) continue;
-      const float wk = w[k] / z;
+    for (int k = 0; k < 7; ++k) {  // unrolled: the record and ls are indexed statically (registers)
+      if (k >= n) break;
+      const float w = __expf(ls[k] - base) / z;
+      if (w == 0.f) continue;
+      const float4* src = reinterpret_cast<const float4*>(p.o_part + prow_of(static_cast<int>(rec[1 + k])) * kDL);
+      float4 v[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[q].x += wk * ov[k][q].x; acc[q].y += wk * ov[k][q].y;
-        acc[q].z += wk * ov[k][q].z; acc[q].w += wk * ov[k][q].w;
-      }
+      for (int q = 0; q < 4; ++q) v[q] = src[lane + 32 * q];
+      add(w, v);
     }
   } else {
     // more pieces (a request spanning many slices): walk the clusters whose
@@ -1543,28 +1564,24 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(Params p) {
     float mx = -INFINITY;
     for (int c = clo; c <= chi; ++c) {
       if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
-      const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
-      mx = fmaxf(mx, p.lse_part[(static_cast<int64_t>(slot) * p.G + g) * kRows + r]);
+      mx = fmaxf(mx, p.lse_part[prow_of(2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0))]);
     }
     base = (mx == -INFINITY) ? 0.f : mx;
     z = 0.f;
     for (int c = clo; c <= chi; ++c) {
       if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
-      const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
-      z += __expf(p.lse_part[(static_cast<int64_t>(slot) * p.G + g) * kRows + r] - base);
+      z += __expf(p.lse_part[prow_of(2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0))] - base);
     }
     for (int c = clo; c <= chi; ++c) {
       if (p.cinfo[3 * c] == p.cinfo[3 * c + 1]) continue;
-      const int slot = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
-      const int64_t prow = (static_cast<int64_t>(slot) * p.G + g) * kRows + r;
+      const int64_t prow = prow_of(2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0));
       const float w = __expf(p.lse_part[prow] - base) / z;
       if (w == 0.f) continue;
       const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * kDL);
+      float4 v[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 v = src[lane + 32 * k];
-        acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
-      }
+      for (int q = 0; q < 4; ++q) v[q] = src[lane + 32 * q];
+      add(w, v);
     }
   }
   const int i = rr / p.H, h = rr % p.H;
