@@ -37,12 +37,12 @@ cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, cudaStrea
 }
 
 // Workspace: [status words | page prefix sums | cluster slices | each
-// request's first and last cluster | each request's pieces and their
-// partial slots | the requests cut into pieces | fp32 partial outputs |
-// partial log-sum-exps | e4m3 query scales].  Sized by B, the cluster count
-// and the number of row blocks only.
+// request's first and last cluster | the requests cut into pieces, each with
+// its pieces' partial slots | fp32 partial outputs | partial log-sum-exps |
+// e4m3 query scales].  Sized by B, the cluster count and the number of row
+// blocks only.
 struct Layout {
-  size_t status, prefix, cinfo, rrange, pieces, splits, o_part, lse_part, qscale, total;
+  size_t status, prefix, cinfo, rrange, splits, o_part, lse_part, qscale, total;
 };
 
 Layout workspace_layout(int B, int C, int G) {
@@ -51,9 +51,8 @@ Layout workspace_layout(int B, int C, int G) {
   l.prefix = 256;
   l.cinfo = l.prefix + align256(static_cast<size_t>(B + 1) * 4);
   l.rrange = l.cinfo + align256(static_cast<size_t>(C) * 3 * 4);
-  l.pieces = l.rrange + align256(static_cast<size_t>(B) * 2 * 4);
-  l.splits = l.pieces + align256(static_cast<size_t>(B) * 8 * 4);
-  l.o_part = l.splits + align256(static_cast<size_t>(1 + (B < C ? B : C)) * 4);
+  l.splits = l.rrange + align256(static_cast<size_t>(B) * 2 * 4);
+  l.o_part = l.splits + align256(static_cast<size_t>(1 + (B < C ? B : C)) * 8 * 4);
   l.lse_part = l.o_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * mla::kDL * 4);
   l.qscale = l.lse_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * 4);
   l.total = l.qscale + align256(static_cast<size_t>(B) * G * mla::kRows * 4);  // e4m3 query scales
@@ -286,7 +285,6 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
   p.cinfo = reinterpret_cast<int32_t*>(ws + lay.cinfo);
   p.rrange = reinterpret_cast<int32_t*>(ws + lay.rrange);
-  p.pieces = reinterpret_cast<int32_t*>(ws + lay.pieces);
   p.splits = reinterpret_cast<int32_t*>(ws + lay.splits);
   p.qscale = reinterpret_cast<float*>(ws + lay.qscale);
   p.B = d->batch;
@@ -591,6 +589,15 @@ extern "C" int mla_trace_kernel_times(void* host_dst, int reset) {
   if (reset) {
     unsigned long long init[8] = {0, 0, ~0ull, 0, ~0ull, ~0ull, 0, 0};
     if (cudaMemcpyToSymbol(mla::g_mla_kernel_times, init, sizeof(init)) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+extern "C" int mla_trace_combine_times(void* host_dst, int reset) {
+  if (cudaMemcpyFromSymbol(host_dst, mla::g_mla_combine_times, sizeof(mla::g_mla_combine_times)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (reset) {
+    static unsigned long long zeros[4096][4];
+    if (cudaMemcpyToSymbol(mla::g_mla_combine_times, zeros, sizeof(zeros)) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return MLA_OK;
 }

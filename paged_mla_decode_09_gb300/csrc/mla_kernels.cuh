@@ -209,8 +209,8 @@ struct Params {
   int32_t* prefix;         // [B+1] page prefix sums
   int32_t* cinfo;          // [C][3] = slice start, slice end, first request
   int32_t* rrange;         // [B][2] = first and last cluster whose slice meets the request
-  int32_t* pieces;         // [B][8] = number of pieces, then the partial slots of the first 7 in order
-  int32_t* splits;         // [1 + min(B, C)] = count, then the requests cut into pieces (any order)
+  int32_t* splits;         // [8] count, then [min(B, C)][8] = (request, pieces, partial slots of the first 6)
+                           // for each request cut into pieces (any order)
   float* qscale;           // [B * R] e4m3 query scales (e4m3 cache only)
   int32_t B, H, Q, R, G, C;
   int32_t num_pages, max_pages, pt_stride;
@@ -234,6 +234,18 @@ __device__ int g_mla_trace_cid;  // the cluster whose events are stamped
 // (after its wait), [3] last combine block exit, [4] first attention CTA
 // entry, [5] first attention CTA past its wait
 __device__ unsigned long long g_mla_kernel_times[8];
+// combine blocks: [block][0] past the wait, [1] record loaded, [2] partials
+// loaded, [3] stored (first warp of the block)
+__device__ unsigned long long g_mla_combine_times[4096][4];
+#define MLA_COMBINE_STAMP(k)                                                  \
+  do {                                                                        \
+    const unsigned bid = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z); \
+    if (threadIdx.x == 0 && bid < 4096) g_mla_combine_times[bid][(k)] = globaltimer_ns(); \
+  } while (0)
+#else
+#define MLA_COMBINE_STAMP(k) \
+  do {                       \
+  } while (0)
 #endif
 #if defined(MLA_TRACE) && !defined(MLA_TRACE_NO_PAGES)
 #define MLA_TRACE_POINT(role, ev, j)                                                                     \
@@ -377,23 +389,25 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     p.rrange[2 * b + 1] = pb1 > pb0 ? lo : 0;
     // the request's pieces in cluster order (empty slices hold none) and
     // their partial slots: 2c for the piece that starts cluster c's slice,
-    // 2c + 1 for a later one; the combine reads these directly
+    // 2c + 1 for a later one.  A request cut into pieces gets an entry of
+    // the combine's list: (b, pieces, the first 6 slots).
     int n = 0;
-    int32_t rec[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int32_t rec[8] = {b, 0, 0, 0, 0, 0, 0, 0};
     if (pb1 > pb0 && lo > clo) {
       for (int c = clo; c <= lo; ++c) {
         const int s = c_ok ? cs[c] : p.cinfo[3 * c], e = c_ok ? ce[c] : p.cinfo[3 * c + 1];
         if (s == e) continue;
         const int f = c_ok ? cf[c] : p.cinfo[3 * c + 2];
-        if (n < 7) rec[1 + n] = 2 * c + (b != f ? 1 : 0);
+        if (n < 6) rec[2 + n] = 2 * c + (b != f ? 1 : 0);
         ++n;
       }
     }
-    rec[0] = n;
-    int4* dst = reinterpret_cast<int4*>(p.pieces + 8 * static_cast<int64_t>(b));
-    dst[0] = make_int4(rec[0], rec[1], rec[2], rec[3]);
-    dst[1] = make_int4(rec[4], rec[5], rec[6], rec[7]);
-    if (n > 1) p.splits[1 + atomicAdd(&nsplit, 1)] = b;  // at most min(B, C - 1) requests
+    rec[1] = n;
+    if (n > 1) {  // at most min(B, C - 1) requests
+      int4* dst = reinterpret_cast<int4*>(p.splits + 8 * (1 + static_cast<int64_t>(atomicAdd(&nsplit, 1))));
+      dst[0] = make_int4(rec[0], rec[1], rec[2], rec[3]);
+      dst[1] = make_int4(rec[4], rec[5], rec[6], rec[7]);
+    }
   }
   __syncthreads();
   if (tid == 0) p.splits[0] = nsplit;
@@ -1483,7 +1497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // batch's combine ran in three and a half waves).
 constexpr int kCombineWarps = 4;
 
-__global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(Params p) {
+__global__ void __launch_bounds__(kCombineWarps * 32, 8) mla_combine_kernel(Params p) {
   griddep_wait();  // the attention kernel's partials (and the schedule) are complete
 #ifdef MLA_TRACE
   if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[2], globaltimer_ns());
@@ -1493,17 +1507,21 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(Params 
     }
   } exit_stamp;
 #endif
-  // block x: the x-th request cut into pieces (the schedule's list), row
-  // block y, rows 4z .. 4z + 3 (one warp each)
-  if (static_cast<int>(blockIdx.x) >= p.splits[0]) return;
-  const int b = p.splits[1 + blockIdx.x], g = blockIdx.y;
+  // block x: entry x of the schedule's list of requests cut into pieces,
+  // row block y, rows 4z .. 4z + 3 (one warp each); the entry (request,
+  // pieces, slots) and the list's length are loaded together
+  MLA_COMBINE_STAMP(0);
+  const int nsplit = p.splits[0];
+  uint32_t ent[8];
+  ldg_v8(p.splits + 8 * (1 + static_cast<int64_t>(blockIdx.x)), ent);
+  if (static_cast<int>(blockIdx.x) >= nsplit) return;
+  const int b = static_cast<int>(ent[0]), g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.z * kCombineWarps + warp;
   const int rr = g * kRows + r;
   if (rr >= p.R) return;
-  uint32_t rec[8];
-  ldg_v8(p.pieces + 8 * static_cast<int64_t>(b), rec);
-  const int n = static_cast<int>(rec[0]);
+  const int n = static_cast<int>(ent[1]);  // pieces; ent[2 + k]: the slot of piece k
+  MLA_COMBINE_STAMP(1);
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1517,7 +1535,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(Params 
   };
   if (n == 2) {
     // the common case: both pieces' lse and partial rows in flight at once
-    const int64_t p0 = prow_of(static_cast<int>(rec[1])), p1 = prow_of(static_cast<int>(rec[2]));
+    const int64_t p0 = prow_of(static_cast<int>(ent[2])), p1 = prow_of(static_cast<int>(ent[3]));
     const float l0 = p.lse_part[p0], l1 = p.lse_part[p1];
     float4 v0[4], v1[4];
     const float4* s0 = reinterpret_cast<const float4*>(p.o_part + p0 * kDL);
@@ -1529,29 +1547,33 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(Params 
     }
     const float mx = fmaxf(l0, l1);
     base = (mx == -INFINITY) ? 0.f : mx;
+#ifdef MLA_TRACE
+    if (v0[0].x == 12345.f && v1[0].x == 12345.f) base += 0.f;  // keeps the loads before the stamp
+#endif
+    MLA_COMBINE_STAMP(2);
     const float w0 = __expf(l0 - base), w1 = __expf(l1 - base);
     z = w0 + w1;
     if (w0 != 0.f) add(w0 / z, v0);
     if (w1 != 0.f) add(w1 / z, v1);
-  } else if (n <= 7) {
+  } else if (n <= 6) {
     // the record's slots: all lse first, then the partial rows one by one
-    float ls[7];
+    float ls[6];
     float mx = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 7; ++k) {
-      ls[k] = k < n ? p.lse_part[prow_of(static_cast<int>(rec[1 + k]))] : -INFINITY;
+    for (int k = 0; k < 6; ++k) {
+      ls[k] = k < n ? p.lse_part[prow_of(static_cast<int>(ent[2 + k]))] : -INFINITY;
       mx = fmaxf(mx, ls[k]);
     }
     base = (mx == -INFINITY) ? 0.f : mx;
     z = 0.f;
 #pragma unroll
-    for (int k = 0; k < 7; ++k) z += k < n ? __expf(ls[k] - base) : 0.f;
+    for (int k = 0; k < 6; ++k) z += k < n ? __expf(ls[k] - base) : 0.f;
 #pragma unroll
-    for (int k = 0; k < 7; ++k) {  // unrolled: the record and ls are indexed statically (registers)
+    for (int k = 0; k < 6; ++k) {  // unrolled: the entry and ls are indexed statically (registers)
       if (k >= n) break;
       const float w = __expf(ls[k] - base) / z;
       if (w == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(p.o_part + prow_of(static_cast<int>(rec[1 + k])) * kDL);
+      const float4* src = reinterpret_cast<const float4*>(p.o_part + prow_of(static_cast<int>(ent[2 + k])) * kDL);
       float4 v[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) v[q] = src[lane + 32 * q];
@@ -1601,6 +1623,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(Params 
     dst[lane + 32 * k] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
   }
   if (lane == 0) p.lse[orow] = base + __logf(z);
+  MLA_COMBINE_STAMP(3);
 }
 
 // ------------------------------------------------------ gather test hook
