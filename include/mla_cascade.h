@@ -21,8 +21,11 @@
  *      after the prefix (lengths seq_lens[b] - prefix_pages * 64, causal
  *      between drafts as usual);
  *   3. a merge of the two (out, lse) per query row by log-sum-exp (the
- *      split-KV merge: section 完整技术清单 > MLA).
- * The three run on `stream` in this order.  Conventions as in mla_decode.h.
+ *      split-KV merge: section 完整技术清单 > MLA), which also checks that
+ *      every row's prefix columns equal row 0's.
+ * The passes keep their results in fp32 until the merge, which rounds to
+ * bf16 once.  The three run on `stream` in this order.  Conventions as in
+ * mla_decode.h.
  */
 #ifndef MLA_CASCADE_H_
 #define MLA_CASCADE_H_

@@ -249,7 +249,8 @@ int check_call(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
 int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
                 const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
                 void* out, float* lse, uint8_t* ws, size_t ws_bytes, bool shrink_to_fit, int32_t* status_out,
-                void* stream_v, void* const* events, bool out_f32 = false) {
+                void* stream_v, void* const* events, bool out_f32 = false, int32_t len_offset = 0,
+                int32_t len_fixed = 0) {
   int rc = check_call(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, status_out);
   if (rc != MLA_OK) return rc;
   if (!ws) return MLA_ERR_INVALID_ARG;
@@ -296,8 +297,10 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.num_pages = d->num_pages;
   p.max_pages = d->max_pages_per_req;
   p.pt_stride = d->page_table_stride;
-  p.unit_cost = mla::unit_cost_pages(f8, R < mla::kRows ? R : mla::kRows);
+  p.unit_cost = mla::unit_cost_pages(f8);
   p.out_f32 = out_f32 ? 1 : 0;
+  p.len_offset = len_offset;
+  p.len_fixed = len_fixed;
   p.scale = scale;
   p.kv_scale = f8 ? kv_scale : 1.f;
   p.timeout_ns = kTimeoutNs;
@@ -414,11 +417,13 @@ int mla_decode_profiled(const mla_dims* d, const void* q_nope, const void* q_pe,
 }
 
 int mla_decode_f32_out(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
-                       const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale,
-                       float kv_scale, float* out, float* lse, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+                       const int32_t* page_table, const int32_t* seq_lens, int32_t len_offset, int32_t len_fixed,
+                       int32_t q_len, float scale, float kv_scale, float* out, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (len_offset < 0 || len_fixed < 0) return MLA_ERR_INVALID_ARG;
   return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse,
-                     static_cast<uint8_t*>(workspace), workspace_bytes, false, nullptr, stream, nullptr, true);
+                     static_cast<uint8_t*>(workspace), workspace_bytes, false, nullptr, stream, nullptr, true,
+                     len_offset, len_fixed);
 }
 
 int mla_query_status(const void* workspace, void* stream_v, int32_t* device_status) {

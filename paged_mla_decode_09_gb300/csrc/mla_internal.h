@@ -11,10 +11,13 @@ extern "C" {
 
 // mla_decode writing fp32 out [B][q_len][H][512] (32-byte aligned) instead
 // of bf16: the cascade's passes keep their partial results unrounded until
-// their merge.
+// their merge.  Request b's length is seq_lens[b] - len_offset, or len_fixed
+// for every request when len_fixed > 0 (seq_lens is then not read): the
+// cascade's suffix pass and prefix pass, without a kernel to rewrite the
+// lengths.
 __attribute__((visibility("hidden"))) int mla_decode_f32_out(
     const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache, const int32_t* page_table,
-    const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale, float* out, float* lse, void* workspace,
-    size_t workspace_bytes, void* stream);
+    const int32_t* seq_lens, int32_t len_offset, int32_t len_fixed, int32_t q_len, float scale, float kv_scale,
+    float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 }  // extern "C"

@@ -56,9 +56,10 @@ constexpr uint32_t kSCol0 = 320;  // TMEM column of S buffer 0 (queries use 0..2
 constexpr int kCtrlBytes = 512;
 // Schedule weight of starting a request piece, in pages: a cluster pays a
 // fixed cost per piece it starts (queries into TMEM, pipeline refill,
-// epilogue).  Measured on GB300: about 6 pages' time for row blocks of at
-// most 64 rows (bf16), about 10 for larger blocks and for e4m3.
-__host__ __device__ constexpr int unit_cost_pages(bool f8, int rows) { return (!f8 && rows <= 64) ? 6 : 10; }
+// epilogue).  Measured on GB300 (per-cluster times against pages and
+// pieces): about 6 pages' time with a bf16 cache, about 10 with e4m3 (whose
+// queries are split into two e4m3 terms at each piece's start).
+__host__ __device__ constexpr int unit_cost_pages(bool f8) { return f8 ? 10 : 6; }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Lazy output rescale: O is rescaled only when a row's running max grows by
@@ -216,6 +217,8 @@ struct Params {
   int32_t num_pages, max_pages, pt_stride;
   int32_t unit_cost;       // schedule weight of a request piece, in pages
   int32_t out_f32;         // out is fp32 [B][Q][H][512] instead of bf16 (internal: the cascade's passes)
+  int32_t len_offset;      // request b's length is seq_lens[b] - len_offset (internal: the cascade's suffix pass)
+  int32_t len_fixed;       // > 0: every request's length, seq_lens unread (internal: the cascade's prefix pass)
   float scale, kv_scale;
   uint64_t timeout_ns;
 };
@@ -259,6 +262,11 @@ __device__ unsigned long long g_mla_combine_times[4096][4];
   } while (0)
 #endif
 
+// Request b's length as this call sees it (see len_offset, len_fixed).
+__device__ __forceinline__ int req_len(const int32_t* seq_lens, int b, int len_offset, int len_fixed) {
+  return len_fixed > 0 ? len_fixed : seq_lens[b] - len_offset;
+}
+
 __device__ __forceinline__ int clamp_len(int L, int max_pages) {
   return L < 0 ? 0 : (L > max_pages * kPage ? max_pages * kPage : L);
 }
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     const int b = base + tid;
     int np = 0;
     if (b < p.B) {
-      const int L = p.seq_lens[b];
+      const int L = req_len(p.seq_lens, b, p.len_offset, p.len_fixed);
       if (L < p.Q || L > p.max_pages * kPage) atomicOr(p.status, MLA_DEV_BAD_SEQ_LEN);
       np = (clamp_len(L, p.max_pages) + kPage - 1) / kPage;
     }
@@ -457,10 +465,12 @@ struct Unit {
 struct UnitIter {
   const int32_t* prefix;
   const int32_t* seq_lens;
-  int B, s, e, b, bfirst, cid, max_pages;
+  int B, s, e, b, bfirst, cid, max_pages, len_offset, len_fixed;
   __device__ void init(const Params& p, int c) {
     prefix = p.prefix;
     seq_lens = p.seq_lens;
+    len_offset = p.len_offset;
+    len_fixed = p.len_fixed;
     B = p.B;
     max_pages = p.max_pages;
     cid = c;
@@ -482,7 +492,7 @@ struct UnitIter {
         u.p0 = p0;
         u.p1 = p1;
         u.np = pb1 - pb0;
-        u.L = clamp_len(seq_lens[bb], max_pages);
+        u.L = clamp_len(req_len(seq_lens, bb, len_offset, len_fixed), max_pages);
         u.slot = (p0 > 0 || p1 < u.np) ? 2 * cid + (bb != bfirst ? 1 : 0) : -1;
         return true;
       }
