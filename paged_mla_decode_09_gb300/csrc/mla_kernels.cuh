@@ -339,6 +339,9 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     sp[0] = 0;
   }
   __syncthreads();
+#ifdef MLA_TRACE
+  if (tid == 0) g_mla_kernel_times[6] = globaltimer_ns();  // lengths loaded and scanned
+#endif
   const int32_t* pre = sp_ok ? sp : p.prefix;
   // Cluster slices are cut in a weighted order: request b occupies
   // p.unit_cost start-up units and then its pages, so clusters whose
@@ -375,6 +378,9 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     }
   }
   __syncthreads();
+#ifdef MLA_TRACE
+  if (tid == 0) g_mla_kernel_times[7] = globaltimer_ns();  // cluster slices written
+#endif
   // per request, the clusters whose slice [s, e) meets its pages
   // [prefix[b], prefix[b+1]): from the first with e > prefix[b] to the last
   // with s < prefix[b+1] (both bounds are non-decreasing in the cluster
