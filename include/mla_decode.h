@@ -171,13 +171,13 @@ int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream
  *     A device reset (cudaDeviceReset, a primary-context reset) loads the
  *     library's device code again: the next call looks the address up
  *     again, so it too belongs outside a capture.
- *   - The call runs on fewer clusters when the split partials of all the
- *     device's clusters would not fit in 16 MiB (each cluster needs about
- *     G * 0.5 MiB, G = ceil(num_heads * q_len / 128): at most about 31
- *     clusters with G = 1 and 15 with G = 2, against 76 and 36 for
- *     mla_decode on GB300), so large batches decode more slowly than with
- *     mla_decode; if even one cluster's partials do not fit (very large
- *     batches), it returns MLA_ERR_SCRATCH_TOO_SMALL.
+ *   - The call splits the keys into fewer slices when the split partials of
+ *     all the slices the device could run at once would not fit in 16 MiB
+ *     (each slice needs about G * 0.5 MiB, G = ceil(num_heads * q_len /
+ *     128): at most about 31 slices with G = 1 and 15 with G = 2, against 76
+ *     and 38 for mla_decode on GB300), so large batches decode more slowly
+ *     than with mla_decode; if even one slice's partials do not fit (very
+ *     large batches), it returns MLA_ERR_SCRATCH_TOO_SMALL.
  *   - All calls share the one array, which keeps the last call's contents:
  *     calls that may overlap on the GPU (other streams, other threads)
  *     race and must be serialised by the caller.
@@ -192,7 +192,8 @@ int mla_decode_noalloc(const mla_dims* d, const void* q_nope, const void* q_pe, 
 const char* mla_status_string(int status);
 
 /* Number of clusters and CTAs per cluster the attention kernel launches for
- * `d` on `device` (reported by the benchmark). */
+ * `d` on `device` (reported by the benchmark): clusters of one S/O CTA pair,
+ * G of them per slice of the work (G = ceil(num_heads * q_len / 128)). */
 int mla_decode_launch_shape(const mla_dims* d, int device, int32_t* clusters, int32_t* cluster_size);
 
 #ifdef __cplusplus

@@ -84,7 +84,9 @@ int device_ok(int device) {
   return MLA_OK;
 }
 
-// Clusters of 2*G CTAs (one S/O pair per row block) that fit at once.
+// Slices of the attention kernel's work: the clusters of one S/O pair that
+// fit at once, divided by G (each slice is computed by G clusters, one per
+// row block).
 struct ShapeCache {
   std::mutex mu;
   int clusters[64][2][3] = {};  // [device][fp8][G]
@@ -113,17 +115,18 @@ int launch_shape(int device, bool f8, int G, int* clusters_out) {
       rc = MLA_ERR_CUDA;
     } else {
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * G * 64, 1, 1);
+      cfg.gridDim = dim3(2 * 64, 1, 1);
       cfg.blockDim = dim3(mla::kThreads, 1, 1);
       cfg.dynamicSmemBytes = smem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2 * G;
+      attr[0].val.clusterDim.x = 2;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) rc = MLA_ERR_CUDA;
+      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < G) rc = MLA_ERR_CUDA;
+      n /= G;
     }
   }
   if (prev != device) cudaSetDevice(prev);
@@ -322,13 +325,13 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   if (!mark(1)) return MLA_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * G * C, 1, 1);
+  cfg.gridDim = dim3(2 * G * C, 1, 1);  // G clusters of one S/O pair per slice
   cfg.blockDim = dim3(mla::kThreads, 1, 1);
   cfg.dynamicSmemBytes = f8 ? Cfg<true>::kSmem : Cfg<false>::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2 * G;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // prologue overlaps the schedule
@@ -387,8 +390,8 @@ int mla_decode_launch_shape(const mla_dims* d, int device, int32_t* clusters, in
   int n = 0;
   rc = launch_shape(device, d->kv_dtype == MLA_KV_FP8_E4M3, G, &n);
   if (rc != MLA_OK) return rc;
-  *clusters = n;
-  *cluster_size = 2 * G;
+  *clusters = n * G;
+  *cluster_size = 2;
   return MLA_OK;
 }
 

@@ -9,7 +9,8 @@
 // "推理优化" tag page (same result as plain attention).
 //
 // GB300 design (one row block = up to 128 query rows = heads x drafts):
-//   * a thread-block cluster holds one CTA PAIR per row block;
+//   * a thread-block cluster is one CTA PAIR; with G row blocks, G clusters
+//     compute the same slice of pages, one row block each;
 //   * the S CTA keeps the row block's absorbed queries in TMEM and computes
 //     S = Q K^T per 64-token page with tcgen05 (A from TMEM, B = the page,
 //     K-major), then the online softmax (one thread per row) and writes the
@@ -548,13 +549,12 @@ __device__ __forceinline__ int q_entries(int rows_real) { return (rows_real + 63
 template <bool kF8, bool kRoleS>
 __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const CUtensorMap* tm_kv,
                              const CUtensorMap* tm_pe, const CUtensorMap* tm_qn, const CUtensorMap* tm_qp, int cid,
-                             uint32_t partner) {
+                             int g, uint32_t partner) {
   using C = Cfg<kF8>;
   constexpr int kNSt = kRoleS ? C::kNStS : C::kNStO;
   constexpr int kSlot = kRoleS ? C::kSlotS : C::kSlotO;
   constexpr uint32_t kCopyBytes = static_cast<uint32_t>((kRoleS ? C::kBoxesPartS : C::kBoxesPartO) * C::kBox);
   volatile int* abort = &ctrl->abort;
-  const int g = static_cast<int>(cluster_ctarank() >> 1);
   const int rows_real = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
   const int qe = (kRoleS && !kF8) ? q_entries(rows_real) : 0;
   UnitIter it;
@@ -863,11 +863,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* data = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(data + C::kData);
+  // one S/O pair per cluster; cluster k computes row block g = k mod G of
+  // slice k / G (the pairs of a slice share nothing but the pages they read)
   const uint32_t rank = cluster_ctarank();
-  const bool role_s = (rank & 1) == 0;
-  const int g = static_cast<int>(rank >> 1);
+  const bool role_s = rank == 0;
   const uint32_t partner = rank ^ 1u;
-  const int cid = static_cast<int>(cluster_id_x());
+  const int clus = static_cast<int>(cluster_id_x());
+  const int g = clus % p.G;
+  const int cid = clus / p.G;  // the slice
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #ifdef MLA_TRACE
   if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[4], globaltimer_ns());
@@ -921,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctrl->tmem_base;
   volatile int* abort = &ctrl->abort;
 #ifdef MLA_TRACE
-  if (threadIdx.x == 0 && rank == 0 && cid < 1024) g_mla_cluster_times[cid][0] = globaltimer_ns();
+  if (threadIdx.x == 0 && rank == 0 && clus < 1024) g_mla_cluster_times[clus][0] = globaltimer_ns();
   if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[5], globaltimer_ns());
 #endif
 
@@ -929,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =========================== S CTA ===========================
     uint8_t* ring = data;
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, &tm_qn, &tm_qp, cid, partner);
+      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, &tm_qn, &tm_qp, cid, g, partner);
     } else if (warp == 1) {
       // QK issuer: the whole warp runs the loop and one elected lane issues
       // (a converged warp keeps the tensor pipe full with N = 64 MMAs), so
@@ -1276,7 +1279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows_real = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
     const PSlots ps(kF8, rows_real);
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, &tm_qn, &tm_qp, cid, partner);
+      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, &tm_qn, &tm_qp, cid, g, partner);
     } else if (warp == 1) {
       // ---- PV warp: for page j it waits until the page is ready for PV
       // (c_kv landed, P arrived, O free on a unit's first page: the
@@ -1497,7 +1500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
 #ifdef MLA_TRACE
-  if (threadIdx.x == 0 && cid < 1024) g_mla_cluster_times[cid][1 + (rank & 1)] = globaltimer_ns();
+  if (threadIdx.x == 0 && clus < 1024) g_mla_cluster_times[clus][1 + (rank & 1)] = globaltimer_ns();
 #endif
   if (warp == 2) tmem_dealloc(tmem, 512);
   cluster_sync();
