@@ -277,6 +277,11 @@ __device__ __forceinline__ int clamp_len(int L, int max_pages) {
 // [T*c/C, T*(c+1)/C) with the request holding its first page.
 constexpr int kSchedSmemB = 4096;     // requests whose prefix sums the schedule keeps in shared memory
 constexpr int kSchedSmemC = 512;      // clusters whose slices it keeps there
+// What cutting requests into pieces costs beyond the pieces' start-up, in
+// pages: the combine kernel's launch and wait, and the fp32 partials that
+// each piece writes and the combine reads back (a 128-row partial is 256 KB,
+// about three and a half bf16 pages, each way).
+constexpr int kSplitPenaltyPages = 8;
 
 __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   __shared__ int32_t warp_tot[32];
@@ -287,6 +292,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   __shared__ int32_t sp[kSchedSmemB + 1];
   __shared__ int32_t cs[kSchedSmemC], ce[kSchedSmemC], cf[kSchedSmemC];
   __shared__ int32_t nsplit;
+  __shared__ int32_t maxnp;
   const bool sp_ok = p.B <= kSchedSmemB;
   const bool c_ok = p.C <= kSchedSmemC;
   griddep_launch_dependents();  // the next kernels wait for this one before reading its output
@@ -297,6 +303,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   if (tid == 0) {
     carry = 0;
     nsplit = 0;
+    maxnp = 0;
   }
   // the status words start each call at zero: nothing writes them before
   // this kernel, and every later writer waits for it (griddep_wait)
@@ -310,6 +317,9 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
       if (L < p.Q || L > p.max_pages * kPage) atomicOr(p.status, MLA_DEV_BAD_SEQ_LEN);
       np = (clamp_len(L, p.max_pages) + kPage - 1) / kPage;
     }
+    int m = np;  // the longest request
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((tid & 31) == 0 && m > 0) atomicMax(&maxnp, m);
     int v = np;  // block-wide inclusive scan
     for (int o = 1; o < 32; o <<= 1) {
       const int t = __shfl_up_sync(0xffffffffu, v, o);
@@ -361,13 +371,26 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     off = off < 0 ? 0 : (off > np ? np : off);
     return static_cast<int>(pre[lo] + off);
   };
+  // A batch of no more requests than slices whose longest request costs
+  // about an even slice gets one request per slice instead: nothing is cut
+  // into pieces, so no partials are written and nothing is merged.
+  const bool whole = p.B <= p.C && (static_cast<int64_t>(maxnp) + p.unit_cost) * p.C <=
+                                       W + static_cast<int64_t>(kSplitPenaltyPages) * p.C;
   for (int c = tid; c < p.C; c += 1024) {
-    const int s = page_at(W * c / p.C);
-    const int e = page_at(W * (c + 1) / p.C);
-    int lo = 0, hi = p.B - 1;  // last request b with prefix[b] <= s
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= s) lo = mid; else hi = mid - 1;
+    int s, e, lo;
+    if (whole) {  // slice c = request c; the slices past the batch are empty
+      s = c < p.B ? pre[c] : static_cast<int>(T);
+      e = c < p.B ? pre[c + 1] : static_cast<int>(T);
+      lo = c < p.B ? c : p.B - 1;
+    } else {
+      s = page_at(W * c / p.C);
+      e = page_at(W * (c + 1) / p.C);
+      lo = 0;
+      int hi = p.B - 1;  // last request b with prefix[b] <= s
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= s) lo = mid; else hi = mid - 1;
+      }
     }
     p.cinfo[3 * c + 0] = s;
     p.cinfo[3 * c + 1] = e;

@@ -3,10 +3,12 @@
 // workspace, then the paged decode runs over them as B * q_len requests of
 // one draft position each.
 //
-// Workspace: [status | packed lengths | empty flags | packed page table |
-// packed rows | decode workspace].  Packed request b' = b * q_len + i owns pages
-// b' * P .. b' * P + P - 1, P = ceil(topk / 64), and its k-th valid entry is
-// its packed row k.
+// Workspace: [per-block status bits | packed lengths | empty flags | packed
+// page table | packed rows | decode workspace].  The gather's blocks each
+// write their status bits to a word of their own (no word needs clearing
+// first); the closing kernel ORs them into the decode's status word.
+// Packed request b' = b * q_len + i owns pages b' * P .. b' * P + P - 1,
+// P = ceil(topk / 64), and its k-th valid entry is its packed row k.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -47,13 +49,17 @@ __global__ void __launch_bounds__(kChunkEntries)
                            int topk, int num_pages, int max_pages, int pt_stride, int p_per,
                            uint8_t* __restrict__ packed, int32_t* __restrict__ packed_pt,
                            int32_t* __restrict__ packed_len, int32_t* __restrict__ packed_empty,
-                           int32_t* status) {
+                           int32_t* __restrict__ block_bits) {
   constexpr int kChunks = kRowBytes / 16;
   constexpr int kPer = (kChunks + 31) / 32;
   __shared__ int warp_cnt[kChunkEntries / 32];
   __shared__ int red[kChunkEntries / 32];
   __shared__ int32_t list_t[kChunkEntries];
   __shared__ int32_t list_slot[kChunkEntries];
+  __shared__ int bits;  // this block's status bits
+  int32_t* status = &bits;
+  if (threadIdx.x == 0) bits = 0;
+  __syncthreads();
   const int bq = blockIdx.y, chunk = blockIdx.x;
   const int b = bq / q_len, i = bq % q_len;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -143,16 +149,26 @@ __global__ void __launch_bounds__(kChunkEntries)
         if (lane + 32 * k < kChunks) dst[lane + 32 * k] = ok[r] ? v[r][k] : make_uint4(0, 0, 0, 0);
     }
   }
+  __syncthreads();
+  if (threadIdx.x == 0) block_bits[static_cast<int64_t>(bq) * gridDim.x + chunk] = bits;
 }
 
-// A (b, i) whose list held no valid entry was decoded over one all-zero
-// key, which leaves out = 0 exactly; its lse becomes that of an empty key
-// set, -inf.  One warp per packed request.
-__global__ void __launch_bounds__(256) mla_topk_empty_kernel(const int32_t* __restrict__ packed_empty, int bq_total,
-                                                             int H, float* __restrict__ lse) {
-  const int bq = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (bq >= bq_total || !packed_empty[bq]) return;
-  for (int h = threadIdx.x & 31; h < H; h += 32) lse[static_cast<int64_t>(bq) * H + h] = -INFINITY;
+// After the decode, one warp per packed request: ORs the gather blocks'
+// status bits of the request into the decode's status word, and gives a
+// (b, i) whose list held no valid entry (decoded over one all-zero key,
+// which leaves out = 0 exactly) the lse of an empty key set, -inf.
+__global__ void __launch_bounds__(256) mla_topk_finish_kernel(const int32_t* __restrict__ block_bits, int nchunk,
+                                                              const int32_t* __restrict__ packed_empty, int bq_total,
+                                                              int H, float* __restrict__ lse, int32_t* status) {
+  const int bq = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (bq >= bq_total) return;
+  int bits = 0;
+  for (int c = lane; c < nchunk; c += 32) bits |= block_bits[static_cast<int64_t>(bq) * nchunk + c];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
+  if (lane == 0 && bits) atomicOr(status, bits);
+  if (!packed_empty[bq]) return;
+  for (int h = lane; h < H; h += 32) lse[static_cast<int64_t>(bq) * H + h] = -INFINITY;
 }
 
 }  // namespace mla
@@ -183,8 +199,8 @@ bool sparse_layout(const mla_dims* d, int32_t topk, int device, SparseLayout* l,
   const size_t dec = mla_decode_workspace_size(pd, device);
   if (dec == 0) return false;
   const size_t row_bytes = d->kv_dtype == MLA_KV_FP8_E4M3 ? 576 : 1152;
-  l->status = 0;
-  l->plen = 256;
+  l->status = 0;  // block status bits: [B * q_len][ceil(topk / 256)]
+  l->plen = align_up(static_cast<size_t>(pd->batch) * ((topk + kChunkEntries - 1) / kChunkEntries) * 4, 256);
   l->pempty = align_up(l->plen + static_cast<size_t>(pd->batch) * 4, 256);
   l->ppt = align_up(l->pempty + static_cast<size_t>(pd->batch) * 4, 256);
   l->rows = align_up(l->ppt + static_cast<size_t>(pd->num_pages) * 4, 1024);
@@ -233,29 +249,31 @@ int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, c
   if (major != 10 || minor != 3) return MLA_ERR_DEVICE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int32_t* status = reinterpret_cast<int32_t*>(ws + l.status);
+  int32_t* block_bits = reinterpret_cast<int32_t*>(ws + l.status);
   int32_t* plen = reinterpret_cast<int32_t*>(ws + l.plen);
   int32_t* pempty = reinterpret_cast<int32_t*>(ws + l.pempty);
   int32_t* ppt = reinterpret_cast<int32_t*>(ws + l.ppt);
   uint8_t* rows = ws + l.rows;
-  if (cudaMemsetAsync(status, 0, 4, stream) != cudaSuccess) return MLA_ERR_CUDA;
   const dim3 grid((topk + kChunkEntries - 1) / kChunkEntries, pd.batch);
   const uint8_t* cache = static_cast<const uint8_t*>(kv_cache);
   if (d->kv_dtype == MLA_KV_FP8_E4M3)
     mla::mla_topk_gather_kernel<576><<<grid, kChunkEntries, 0, stream>>>(
         cache, page_table, seq_lens, indices, d->q_len, topk, d->num_pages, d->max_pages_per_req,
-        d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, pempty, status);
+        d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, pempty, block_bits);
   else
     mla::mla_topk_gather_kernel<1152><<<grid, kChunkEntries, 0, stream>>>(
         cache, page_table, seq_lens, indices, d->q_len, topk, d->num_pages, d->max_pages_per_req,
-        d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, pempty, status);
+        d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, pempty, block_bits);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
   // the packed problem: request b * q_len + i has one draft position; its
   // queries and outputs are those of (b, i), already laid out that way
   const int rc = mla_decode(&pd, q_nope, q_pe, rows, ppt, plen, 1, scale, kv_scale, out, lse, ws + l.dec,
                             workspace_bytes - l.dec, stream_v);
   if (rc != MLA_OK) return rc;
-  mla::mla_topk_empty_kernel<<<(pd.batch + 7) / 8, 256, 0, stream>>>(pempty, pd.batch, d->num_heads, lse);
+  // the decode's status word (cleared by its schedule kernel) collects the gather's bits too
+  mla::mla_topk_finish_kernel<<<(pd.batch + 7) / 8, 256, 0, stream>>>(
+      block_bits, static_cast<int>(grid.x), pempty, pd.batch, d->num_heads, lse,
+      reinterpret_cast<int32_t*>(ws + l.dec));
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -267,12 +285,7 @@ int mla_decode_sparse_query_status(const mla_dims* d, int32_t topk, const void* 
   SparseLayout l;
   mla_dims pd;
   if (!sparse_layout(d, topk, dev, &l, &pd)) return MLA_ERR_INVALID_ARG;
-  int32_t dec_status = 0, gather_status = 0;
-  const int rc = mla_query_status(static_cast<const uint8_t*>(workspace) + l.dec, stream_v, &dec_status);
-  if (rc != MLA_OK) return rc;
-  if (cudaMemcpy(&gather_status, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
-  *status = dec_status | gather_status;
-  return MLA_OK;
+  return mla_query_status(static_cast<const uint8_t*>(workspace) + l.dec, stream_v, status);
 }
 
 }  // extern "C"
