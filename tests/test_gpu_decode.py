@@ -88,6 +88,21 @@ def test_batch_beyond_schedule_shared_copy():
     compare(wl, out, lse, label="B=4200")
 
 
+@pytest.mark.parametrize("B,L,H,Q,dtype", [
+    (76, 2000, 128, 1, "bf16"),     # as many requests as slices
+    (70, 700, 16, 1, "bf16"),       # a few slices left empty
+    (64, 2000, 64, 2, "fp8_e4m3"),  # e4m3 start-up weight, two drafts
+])
+def test_small_batch_one_request_per_slice(B, L, H, Q, dtype):
+    """No more requests than slices, of equal lengths: the schedule gives each
+    request a slice of its own (no request is cut, the combine's list is
+    empty) instead of cutting the pages evenly."""
+    wl = W.custom([L] * B, num_heads=H, q_len=Q, kv_dtype=dtype, seed=B + L + H)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    compare(wl, out, lse, label=f"one-per-slice B={B} L={L} {dtype}")
+
+
 def test_long_pipeline_many_pages_per_cluster():
     """Hundreds of pages per cluster: every pipeline barrier wraps many times
     and output rescales happen on many pages."""
