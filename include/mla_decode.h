@@ -162,7 +162,7 @@ int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream
  * that must not allocate, a process whose device memory is all handed to
  * its own pool, or a plug-in that only receives buffers from its host).
  * Same arguments and results as mla_decode, but there is no workspace: the
- * status words, schedule and split partials live in a static 16 MiB device
+ * status words, schedule and split partials live in a static 40 MiB device
  * array inside this library (every GPU that loads the library holds it
  * until the process exits).  The caller still passes all inputs and
  * outputs.  Nothing is allocated or freed.
@@ -171,13 +171,14 @@ int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream
  *     A device reset (cudaDeviceReset, a primary-context reset) loads the
  *     library's device code again: the next call looks the address up
  *     again, so it too belongs outside a capture.
- *   - The call splits the keys into fewer slices when the split partials of
- *     all the slices the device could run at once would not fit in 16 MiB
- *     (each slice needs about G * 0.5 MiB, G = ceil(num_heads * q_len /
- *     128): at most about 31 slices with G = 1 and 15 with G = 2, against 76
- *     and 38 for mla_decode on GB300), so large batches decode more slowly
- *     than with mla_decode; if even one slice's partials do not fit (very
- *     large batches), it returns MLA_ERR_SCRATCH_TOO_SMALL.
+ *   - Each slice of the work needs about G * 0.5 MiB of split partials
+ *     (G = ceil(num_heads * q_len / 128)), so the 76 slices (G = 1) or 38
+ *     (G = 2) that mla_decode runs on GB300 fit, together with the schedule
+ *     of a batch of up to about two thousand requests: there the call runs
+ *     as fast as mla_decode.  Larger batches leave less room for partials
+ *     and are decoded on fewer slices, more slowly; if even one slice's
+ *     partials do not fit (very large batches), the call returns
+ *     MLA_ERR_SCRATCH_TOO_SMALL.
  *   - All calls share the one array, which keeps the last call's contents:
  *     calls that may overlap on the GPU (other streams, other threads)
  *     race and must be serialised by the caller.

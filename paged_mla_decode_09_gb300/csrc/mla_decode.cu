@@ -377,7 +377,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MLA_ERR_CUDA: return "CUDA error";
     case MLA_ERR_DEVICE: return "device is not sm_103a";
-    case MLA_ERR_SCRATCH_TOO_SMALL: return "dimensions exceed the 16 MiB static scratch of mla_decode_noalloc";
+    case MLA_ERR_SCRATCH_TOO_SMALL: return "dimensions exceed the 40 MiB static scratch of mla_decode_noalloc";
     default: return "unknown status";
   }
 }
@@ -507,7 +507,11 @@ int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream
 // array until the process exits.
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+// 40 MiB: the split partials of every slice a GB300 runs at once (2 slots
+// of 128 x 512 fp32 per slice and row block, 38 MiB) plus the schedule and
+// query scales of a batch of about two thousand requests; larger batches
+// run on fewer slices
+constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch, looked up with the device current (in

@@ -4,7 +4,7 @@ mla_decode_noalloc exists for callers that cannot allocate device memory:
 a serving loop that must never call cudaMalloc, a process that handed all
 device memory to its own pool at start-up, or a plug-in that only receives
 buffers from its host.  It keeps its scratch (status words, schedule, split
-partials) in a fixed 16 MiB array inside the library instead of a caller
+partials) in a fixed 40 MiB array inside the library instead of a caller
 workspace.  Two calls in a row, made through the C ABI, must agree with
 mla_decode and with the CPU oracle within the parity tolerance (they may
 split the keys over fewer clusters, so only rounding may differ) and with
@@ -96,9 +96,9 @@ def test_noalloc_rejects_batches_beyond_its_scratch(lib):
     wl = W.custom([100], num_heads=16, seed=3)
     db = to_device(wl)
     dims = mla.make_dims(db.q_nope, db.kv_cache, db.page_table)
-    dims.batch = 5_000_000  # the schedule alone would need 20 MB: refused before any launch
+    dims.batch = 5_000_000  # the schedule alone would need 60 MB: refused before any launch
     out = torch.empty(1, 1, 16, 512, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(1, 1, 16, dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     assert _noalloc(lib, db, dims, out, lse, status) == -7
-    assert b"16 MiB" in lib.mla_status_string(-7)
+    assert b"40 MiB" in lib.mla_status_string(-7)
