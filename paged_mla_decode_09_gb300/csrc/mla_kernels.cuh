@@ -1540,7 +1540,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kCombineWarps = 4;
 
 __global__ void __launch_bounds__(kCombineWarps * 32, 8) mla_combine_kernel(Params p) {
-  griddep_wait();  // the attention kernel's partials (and the schedule) are complete
+  // block x: entry x of the schedule's list of requests cut into pieces,
+  // row block y, rows 4z .. 4z + 3 (one warp each).  The schedule kernel
+  // ended before the attention kernel began, so its list is read before
+  // waiting for the attention kernel (through L2: an earlier call's list
+  // may sit in this SM's L1); blocks past the list's end leave at once.
+  const int nsplit = __ldcg(p.splits);
+  if (static_cast<int>(blockIdx.x) >= nsplit) return;
+  uint32_t ent[8];
+  ldcg_v8(p.splits + 8 * (1 + static_cast<int64_t>(blockIdx.x)), ent);
+  griddep_wait();  // the attention kernel's partials are complete
 #ifdef MLA_TRACE
   if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[2], globaltimer_ns());
   struct Exit {  // every warp stamps its exit (warps leave at different points)
@@ -1549,14 +1558,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 8) mla_combine_kernel(Para
     }
   } exit_stamp;
 #endif
-  // block x: entry x of the schedule's list of requests cut into pieces,
-  // row block y, rows 4z .. 4z + 3 (one warp each); the entry (request,
-  // pieces, slots) and the list's length are loaded together
   MLA_COMBINE_STAMP(0);
-  const int nsplit = p.splits[0];
-  uint32_t ent[8];
-  ldg_v8(p.splits + 8 * (1 + static_cast<int64_t>(blockIdx.x)), ent);
-  if (static_cast<int>(blockIdx.x) >= nsplit) return;
   const int b = static_cast<int>(ent[0]), g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.z * kCombineWarps + warp;

@@ -197,6 +197,13 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
 }
 
 // 32-byte global accesses (one whole sector per lane); 32-byte aligned addresses.
+// ldcg_v8 reads through L2 only (no possibly stale L1 line).
+__device__ __forceinline__ void ldcg_v8(const void* gaddr, uint32_t (&r)[8]) {
+  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(reinterpret_cast<uint64_t>(gaddr))
+               : "memory");
+}
 __device__ __forceinline__ void ldg_v8(const void* gaddr, uint32_t (&r)[8]) {
   asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
