@@ -459,14 +459,16 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
 // e4m3 cache: per query row r of request b, the scale of its e4m3 split,
 // max |q| / 448 over the 576 values (1 for an all-zero row).  One warp per row.
 __global__ void __launch_bounds__(256) mla_qscale_kernel(Params p) {
-  // needs nothing from the schedule, so it may run beside it; it ends only
-  // after the schedule has (griddep_wait below), so the attention kernel's
-  // wait for this one covers both
+  // needs nothing from the schedule, so it may run beside it; block 0 ends
+  // only after the schedule has (griddep_wait below), so the attention
+  // kernel's wait for this grid covers both.  The other blocks leave as soon
+  // as they are done: had each of them waited, the first waves would hold
+  // their SMs until the schedule ended and the later ones would queue.
   griddep_launch_dependents();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<int64_t>(p.B) * p.R) {
-    griddep_wait();
+    if (blockIdx.x == 0) griddep_wait();
     return;
   }
   const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(256) mla_qscale_kernel(Params p) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if (lane == 0) p.qscale[row] = amax > 0.f ? amax / 448.f : 1.f;
-  griddep_wait();
+  if (blockIdx.x == 0) griddep_wait();
 }
 
 // One request's piece inside a cluster's slice.
