@@ -92,6 +92,7 @@ def test_batch_beyond_schedule_shared_copy():
     (76, 2000, 128, 1, "bf16"),     # as many requests as slices
     (70, 700, 16, 1, "bf16"),       # a few slices left empty
     (64, 2000, 64, 2, "fp8_e4m3"),  # e4m3 start-up weight, two drafts
+    (38, 1500, 128, 2, "fp8_e4m3"), # two row blocks per request (two clusters per slice)
 ])
 def test_small_batch_one_request_per_slice(B, L, H, Q, dtype):
     """No more requests than slices, of equal lengths: the schedule gives each
