@@ -113,6 +113,16 @@ def test_long_pipeline_many_pages_per_cluster():
     compare(wl, out, lse, label="long-pipeline")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_single_long_request_over_every_slice(dtype):
+    """One request of 131,072 tokens: every slice holds a piece of it, and
+    the combine merges them all (one piece per cluster)."""
+    wl = W.custom([131072], num_heads=128, q_len=1, kv_dtype=dtype, seed=61)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    compare(wl, out, lse, label=f"131K tokens {dtype}")
+
+
 def test_peaked_softmax():
     """q scaled x4: nearly one-hot weights, where the absolute tolerance term
     cannot hide errors."""
