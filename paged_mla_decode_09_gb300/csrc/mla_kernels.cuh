@@ -1540,8 +1540,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (with 256-thread blocks of ~100 registers only two fit per SM, and a Kimi
 // batch's combine ran in three and a half waves).
 constexpr int kCombineWarps = 4;
+constexpr int kCombineChunks = 3;  // 32 clusters each: requests over up to 96 slices take the lane-parallel path
 
-__global__ void __launch_bounds__(kCombineWarps * 32, 8) mla_combine_kernel(Params p) {
+__global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Params p) {
   // block x: entry x of the schedule's list of requests cut into pieces,
   // row block y, rows 4z .. 4z + 3 (one warp each).  The schedule kernel
   // ended before the attention kernel began, so its list is read before
@@ -1625,9 +1626,69 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 8) mla_combine_kernel(Para
       for (int q = 0; q < 4; ++q) v[q] = src[lane + 32 * q];
       add(w, v);
     }
+  } else if (p.rrange[2 * b + 1] - p.rrange[2 * b] < 32 * kCombineChunks) {
+    // more pieces (a request spanning many slices).  Lane l takes the
+    // clusters clo + l, clo + l + 32, ... whose slice meets the request (an
+    // empty slice holds no piece: weight 0), loads their lse at once and the
+    // warp reduces max and sum; then the warp walks the clusters in order,
+    // weights and slots broadcast, two partial rows in flight.  (A walk
+    // with a load per piece and per pass took ~50 us for one request over
+    // 76 slices.)
+    const int clo = p.rrange[2 * b], chi = p.rrange[2 * b + 1];
+    int slv[kCombineChunks];
+    float lsv[kCombineChunks];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kCombineChunks; ++k) {
+      const int c = clo + 32 * k + lane;
+      slv[k] = 0;
+      lsv[k] = -INFINITY;
+      if (c <= chi && p.cinfo[3 * c] != p.cinfo[3 * c + 1]) {
+        slv[k] = 2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0);
+        lsv[k] = p.lse_part[prow_of(slv[k])];
+      }
+      mx = fmaxf(mx, lsv[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    base = (mx == -INFINITY) ? 0.f : mx;
+    float wv[kCombineChunks];
+    z = 0.f;
+#pragma unroll
+    for (int k = 0; k < kCombineChunks; ++k) {
+      wv[k] = lsv[k] == -INFINITY ? 0.f : __expf(lsv[k] - base);
+      z += wv[k];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+#pragma unroll
+    for (int k = 0; k < kCombineChunks; ++k) wv[k] /= z;
+#pragma unroll
+    for (int k = 0; k < kCombineChunks; ++k) {
+      if (clo + 32 * k > chi) break;
+#pragma unroll 1
+      for (int j = 0; j < 32; j += 2) {
+        float w2[2];
+        int s2[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          w2[q] = __shfl_sync(0xffffffffu, wv[k], j + q);
+          s2[q] = __shfl_sync(0xffffffffu, slv[k], j + q);
+        }
+        float4 v[2][4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float4* src = reinterpret_cast<const float4*>(p.o_part + prow_of(s2[q]) * kDL);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[q][e] = w2[q] != 0.f ? src[lane + 32 * e] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (w2[q] != 0.f) add(w2[q], v[q]);
+      }
+    }
   } else {
-    // more pieces (a request spanning many slices): walk the clusters whose
-    // slice meets it; empty slices hold no piece
+    // more clusters than the lanes take at once: walk them one by one
     const int clo = p.rrange[2 * b], chi = p.rrange[2 * b + 1];
     float mx = -INFINITY;
     for (int c = clo; c <= chi; ++c) {
