@@ -23,10 +23,12 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // while the previous kernel in the stream is finishing and waits for it
 // (griddep_wait) before reading that kernel's output.
 template <typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -90,6 +92,9 @@ int device_ok(int device) {
 struct ShapeCache {
   std::mutex mu;
   int clusters[64][2][3] = {};  // [device][fp8][G]
+  int smem_sm[64] = {};         // shared memory per SM, reserved per block, a block's maximum
+  int smem_rsv[64] = {};
+  int smem_blk[64] = {};
 };
 ShapeCache g_shapes;
 
@@ -129,15 +134,42 @@ int launch_shape(int device, bool f8, int G, int* clusters_out) {
       n /= G;
     }
   }
+  // the combine kernel takes dynamic shared memory that it does not use
+  // (up to a block's maximum) to cap its blocks per SM
+  int smem_sm = 0, smem_rsv = 0, smem_blk = 0;
+  if (rc == MLA_OK &&
+      (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess ||
+       cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, device) != cudaSuccess ||
+       cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess ||
+       cudaFuncSetAttribute(mla::mla_combine_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_blk) !=
+           cudaSuccess ||
+       cudaFuncSetAttribute(mla::mla_combine_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_blk) !=
+           cudaSuccess ||
+       cudaFuncSetAttribute(mla::mla_combine_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_blk) !=
+           cudaSuccess))
+    rc = MLA_ERR_CUDA;
   if (prev != device) cudaSetDevice(prev);
   if (rc != MLA_OK) {
     cudaGetLastError();
     return rc;
   }
   std::lock_guard<std::mutex> lk(g_shapes.mu);
+  g_shapes.smem_sm[device] = smem_sm;
+  g_shapes.smem_rsv[device] = smem_rsv;
+  g_shapes.smem_blk[device] = smem_blk;
   g_shapes.clusters[device][f8][G] = n;
   *clusters_out = n;
   return MLA_OK;
+}
+
+// Dynamic shared memory that lets at most k blocks of a kernel that uses
+// none share an SM (0: no cap).
+size_t spread_smem(int device, int k) {
+  std::lock_guard<std::mutex> lk(g_shapes.mu);
+  if (k >= mla::kCombineBlocksPerSm || g_shapes.smem_sm[device] <= 0) return 0;
+  int s = g_shapes.smem_sm[device] / k - g_shapes.smem_rsv[device];
+  if (s > g_shapes.smem_blk[device]) s = g_shapes.smem_blk[device];
+  return s > 0 ? static_cast<size_t>(s) & ~static_cast<size_t>(127) : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -317,7 +349,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
   if (f8) {  // per-row e4m3 query scales
     if (launch_pdl(mla::mla_qscale_kernel, dim3(static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8)),
-                   dim3(256), stream, p) != cudaSuccess) {
+                   dim3(256), 0, stream, p) != cudaSuccess) {
       cudaGetLastError();
       return MLA_ERR_CUDA;
     }
@@ -353,8 +385,25 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   // rows per row block that exist (R < 128: only the first R)
   const unsigned zrows = static_cast<unsigned>(((R < mla::kRows ? R : mla::kRows) + mla::kCombineWarps - 1) /
                                                mla::kCombineWarps);
-  if (launch_pdl(mla::mla_combine_kernel, dim3(nsplit_max, G, zrows), dim3(mla::kCombineWarps * 32), stream, p) !=
-      cudaSuccess) {
+  // A batch of few requests splits each row's columns over two or four
+  // blocks (more partial rows in flight per warp) while the grid still fits
+  // the GPU at once.  Under programmatic dependent launch the blocks go to
+  // the SMs that the attention kernel frees first, as many to each as fit:
+  // one 131K-token request's 32 blocks, packed onto the first five SMs, took
+  // twice as long as spread over 32.  Shared memory that the kernel does not
+  // use caps the blocks per SM at what spreads the grid over the attention
+  // kernel's SMs.
+  const unsigned sms = 2u * G * C;  // the attention kernel's CTAs, one per SM
+  const unsigned resident = static_cast<unsigned>(mla::kCombineBlocksPerSm) * sms;
+  const unsigned base = nsplit_max * G * zrows;
+  const int parts = base * 4 <= resident ? 4 : base * 2 <= resident ? 2 : 1;
+  const unsigned per_sm = (base * parts + sms - 1) / sms;
+  const size_t csmem = spread_smem(dev, static_cast<int>(per_sm));
+  const dim3 cgrid(nsplit_max, G, zrows * parts), cblock(mla::kCombineWarps * 32);
+  const cudaError_t ce = parts == 4   ? launch_pdl(mla::mla_combine_kernel<4>, cgrid, cblock, csmem, stream, p)
+                         : parts == 2 ? launch_pdl(mla::mla_combine_kernel<2>, cgrid, cblock, csmem, stream, p)
+                                      : launch_pdl(mla::mla_combine_kernel<1>, cgrid, cblock, csmem, stream, p);
+  if (ce != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
   }

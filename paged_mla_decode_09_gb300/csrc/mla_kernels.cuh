@@ -291,6 +291,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   // global arrays
   __shared__ int32_t sp[kSchedSmemB + 1];
   __shared__ int32_t cs[kSchedSmemC], ce[kSchedSmemC], cf[kSchedSmemC];
+  __shared__ int32_t cnz[kSchedSmemC + 1];  // non-empty slices among clusters [0, c)
   __shared__ int32_t nsplit;
   __shared__ int32_t maxnp;
   const bool sp_ok = p.B <= kSchedSmemB;
@@ -401,7 +402,19 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
       cf[c] = lo;
     }
   }
+  // C <= 512: thread c wrote cluster c's slice; a ballot per warp of the
+  // non-empty ones, then each cluster's count of those before it
+  const unsigned m = c_ok ? __ballot_sync(0xffffffffu, tid < p.C && cs[tid] != ce[tid]) : 0u;
+  if (c_ok && (tid & 31) == 0) warp_tot[tid >> 5] = __popc(m);
   __syncthreads();
+  if (c_ok) {
+    if (tid <= p.C) {
+      int k = __popc(m & ((1u << (tid & 31)) - 1u));
+      for (int w = 0; w < (tid >> 5); ++w) k += warp_tot[w];
+      cnz[tid] = k;
+    }
+    __syncthreads();
+  }
 #ifdef MLA_TRACE
   if (tid == 0) g_mla_kernel_times[7] = globaltimer_ns();  // cluster slices written
 #endif
@@ -432,12 +445,20 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     int n = 0;
     int32_t rec[8] = {b, 0, 0, 0, 0, 0, 0, 0};
     if (pb1 > pb0 && lo > clo) {
-      for (int c = clo; c <= lo; ++c) {
-        const int s = c_ok ? cs[c] : p.cinfo[3 * c], e = c_ok ? ce[c] : p.cinfo[3 * c + 1];
-        if (s == e) continue;
-        const int f = c_ok ? cf[c] : p.cinfo[3 * c + 2];
-        if (n < 6) rec[2 + n] = 2 * c + (b != f ? 1 : 0);
-        ++n;
+      auto empty = [&](int c) { return c_ok ? cs[c] == ce[c] : p.cinfo[3 * c] == p.cinfo[3 * c + 1]; };
+      if (c_ok) {
+        n = cnz[lo + 1] - cnz[clo];
+      } else {
+        for (int c = clo; c <= lo; ++c) n += empty(c) ? 0 : 1;
+      }
+      int c = clo;
+#pragma unroll
+      for (int k = 0; k < 6; ++k) {  // unrolled: rec is indexed statically (registers)
+        while (c <= lo && empty(c)) ++c;
+        if (c <= lo) {
+          rec[2 + k] = 2 * c + (b != (c_ok ? cf[c] : p.cinfo[3 * c + 2]) ? 1 : 0);
+          ++c;
+        }
       }
     }
     rec[1] = n;
@@ -1540,14 +1561,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (with 256-thread blocks of ~100 registers only two fit per SM, and a Kimi
 // batch's combine ran in three and a half waves).
 constexpr int kCombineWarps = 4;
+constexpr int kCombineBlocksPerSm = 7;  // 72 registers: seven 128-thread blocks per SM's 64K
 constexpr int kCombineChunks = 3;  // 32 clusters each: requests over up to 96 slices take the lane-parallel path
 
-__global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Params p) {
+// kParts blocks share each quad of rows, block z % kParts merging the
+// z-th of kParts equal column ranges: a batch of few requests gets more
+// blocks, each with more partial rows in flight per warp.
+template <int kParts>
+__global__ void __launch_bounds__(kCombineWarps * 32, kCombineBlocksPerSm) mla_combine_kernel(Params p) {
+  static_assert(kParts == 1 || kParts == 2 || kParts == 4, "a row's 128 float4s split evenly over the lanes");
+  constexpr int kV = 4 / kParts;    // float4s of a row per lane
+  constexpr int kFly = 2 * kParts;  // partial rows in flight in the long walk
   // block x: entry x of the schedule's list of requests cut into pieces,
-  // row block y, rows 4z .. 4z + 3 (one warp each).  The schedule kernel
-  // ended before the attention kernel began, so its list is read before
-  // waiting for the attention kernel (through L2: an earlier call's list
-  // may sit in this SM's L1); blocks past the list's end leave at once.
+  // row block y, rows 4(z / kParts) .. + 3 (one warp each).  The schedule
+  // kernel ended before the attention kernel began, so its list is read
+  // before waiting for the attention kernel (through L2: an earlier call's
+  // list may sit in this SM's L1); blocks past the list's end leave at once.
   const int nsplit = __ldcg(p.splits);
   if (static_cast<int>(blockIdx.x) >= nsplit) return;
   uint32_t ent[8];
@@ -1564,19 +1593,26 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Para
   MLA_COMBINE_STAMP(0);
   const int b = static_cast<int>(ent[0]), g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.z * kCombineWarps + warp;
+  const int part = static_cast<int>(blockIdx.z) % kParts;
+  const int r = (static_cast<int>(blockIdx.z) / kParts) * kCombineWarps + warp;
   const int rr = g * kRows + r;
   if (rr >= p.R) return;
+  const int col = lane + 32 * kV * part;  // this lane's float4s of a row: col, col + 32, ...
   const int n = static_cast<int>(ent[1]);  // pieces; ent[2 + k]: the slot of piece k
   MLA_COMBINE_STAMP(1);
-  float4 acc[4];
+  float4 acc[kV];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < kV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   float base, z;
   auto prow_of = [&](int slot) { return (static_cast<int64_t>(slot) * p.G + g) * kRows + r; };
-  auto add = [&](float w, const float4 (&v)[4]) {
+  auto load = [&](int64_t prow, float4 (&v)[kV]) {
+    const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * kDL);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kV; ++q) v[q] = src[col + 32 * q];
+  };
+  auto add = [&](float w, const float4 (&v)[kV]) {
+#pragma unroll
+    for (int q = 0; q < kV; ++q) {
       acc[q].x += w * v[q].x; acc[q].y += w * v[q].y; acc[q].z += w * v[q].z; acc[q].w += w * v[q].w;
     }
   };
@@ -1584,14 +1620,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Para
     // the common case: both pieces' lse and partial rows in flight at once
     const int64_t p0 = prow_of(static_cast<int>(ent[2])), p1 = prow_of(static_cast<int>(ent[3]));
     const float l0 = p.lse_part[p0], l1 = p.lse_part[p1];
-    float4 v0[4], v1[4];
-    const float4* s0 = reinterpret_cast<const float4*>(p.o_part + p0 * kDL);
-    const float4* s1 = reinterpret_cast<const float4*>(p.o_part + p1 * kDL);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v0[q] = s0[lane + 32 * q];
-      v1[q] = s1[lane + 32 * q];
-    }
+    float4 v0[kV], v1[kV];
+    load(p0, v0);
+    load(p1, v1);
     const float mx = fmaxf(l0, l1);
     base = (mx == -INFINITY) ? 0.f : mx;
 #ifdef MLA_TRACE
@@ -1620,10 +1651,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Para
       if (k >= n) break;
       const float w = __expf(ls[k] - base) / z;
       if (w == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(p.o_part + prow_of(static_cast<int>(ent[2 + k])) * kDL);
-      float4 v[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] = src[lane + 32 * q];
+      float4 v[kV];
+      load(prow_of(static_cast<int>(ent[2 + k])), v);
       add(w, v);
     }
   } else if (p.rrange[2 * b + 1] - p.rrange[2 * b] < 32 * kCombineChunks) {
@@ -1631,7 +1660,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Para
     // clusters clo + l, clo + l + 32, ... whose slice meets the request (an
     // empty slice holds no piece: weight 0), loads their lse at once and the
     // warp reduces max and sum; then the warp walks the clusters in order,
-    // weights and slots broadcast, two partial rows in flight.  (A walk
+    // weights and slots broadcast, kFly partial rows in flight.  (A walk
     // with a load per piece and per pass took ~50 us for one request over
     // 76 slices.)
     const int clo = p.rrange[2 * b], chi = p.rrange[2 * b + 1];
@@ -1667,24 +1696,24 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Para
     for (int k = 0; k < kCombineChunks; ++k) {
       if (clo + 32 * k > chi) break;
 #pragma unroll 1
-      for (int j = 0; j < 32; j += 2) {
-        float w2[2];
-        int s2[2];
+      for (int j = 0; j < 32; j += kFly) {
+        float wf[kFly];
+        int sf[kFly];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          w2[q] = __shfl_sync(0xffffffffu, wv[k], j + q);
-          s2[q] = __shfl_sync(0xffffffffu, slv[k], j + q);
+        for (int q = 0; q < kFly; ++q) {
+          wf[q] = __shfl_sync(0xffffffffu, wv[k], j + q);
+          sf[q] = __shfl_sync(0xffffffffu, slv[k], j + q);
         }
-        float4 v[2][4];
+        float4 v[kFly][kV];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float4* src = reinterpret_cast<const float4*>(p.o_part + prow_of(s2[q]) * kDL);
+        for (int q = 0; q < kFly; ++q) {
+          const float4* src = reinterpret_cast<const float4*>(p.o_part + prow_of(sf[q]) * kDL);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) v[q][e] = w2[q] != 0.f ? src[lane + 32 * e] : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int e = 0; e < kV; ++e) v[q][e] = wf[q] != 0.f ? src[col + 32 * e] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-          if (w2[q] != 0.f) add(w2[q], v[q]);
+        for (int q = 0; q < kFly; ++q)
+          if (wf[q] != 0.f) add(wf[q], v[q]);
       }
     }
   } else {
@@ -1706,10 +1735,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Para
       const int64_t prow = prow_of(2 * c + (b != p.cinfo[3 * c + 2] ? 1 : 0));
       const float w = __expf(p.lse_part[prow] - base) / z;
       if (w == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(p.o_part + prow * kDL);
-      float4 v[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] = src[lane + 32 * q];
+      float4 v[kV];
+      load(prow, v);
       add(w, v);
     }
   }
@@ -1718,18 +1745,18 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 7) mla_combine_kernel(Para
   if (p.out_f32) {
     float4* dstf = reinterpret_cast<float4*>(p.out + orow * kDL * 4);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) dstf[lane + 32 * k] = acc[k];
-    if (lane == 0) p.lse[orow] = base + __logf(z);
+    for (int k = 0; k < kV; ++k) dstf[col + 32 * k] = acc[k];
+    if (lane == 0 && part == 0) p.lse[orow] = base + __logf(z);
     return;
   }
   uint2* dst = reinterpret_cast<uint2*>(p.out + orow * kDL * 2);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < kV; ++k) {
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
     __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-    dst[lane + 32 * k] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    dst[col + 32 * k] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
   }
-  if (lane == 0) p.lse[orow] = base + __logf(z);
+  if (lane == 0 && part == 0) p.lse[orow] = base + __logf(z);
   MLA_COMBINE_STAMP(3);
 }
 

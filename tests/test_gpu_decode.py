@@ -123,6 +123,27 @@ def test_single_long_request_over_every_slice(dtype):
     compare(wl, out, lse, label=f"131K tokens {dtype}")
 
 
+@pytest.mark.parametrize(
+    "lens_seed,H,Q,dtype",
+    [
+        ((12, 6000, 12000), 128, 1, "bf16"),  # each row's columns over 2 combine blocks
+        ((40, 2000, 9000), 64, 1, "bf16"),  # one block per row quad, spread 5 per SM
+        ((3, 20000, 40000), 64, 4, "fp8_e4m3"),  # 4 blocks per row quad, two row blocks
+        ((5, 9000, 30000), 16, 1, "bf16"),  # 4 blocks per row quad, 16 rows
+    ],
+)
+def test_combine_column_parts(lens_seed, H, Q, dtype):
+    """Few requests, each cut into several or many pieces: the combine splits
+    each row's columns over 1, 2 or 4 blocks (every merge branch: two
+    pieces, up to six, the lane-parallel walk)."""
+    n, lo, hi = lens_seed
+    lens = np.random.default_rng(n * 1000 + H).integers(lo, hi, size=n).tolist()
+    wl = W.custom(lens, num_heads=H, q_len=Q, kv_dtype=dtype, seed=62 + n)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    compare(wl, out, lse, label=f"combine parts B={n} H={H} Q={Q} {dtype}")
+
+
 def test_peaked_softmax():
     """q scaled x4: nearly one-hot weights, where the absolute tolerance term
     cannot hide errors."""
