@@ -494,13 +494,20 @@ __global__ void __launch_bounds__(256) mla_qscale_kernel(Params p) {
   }
   const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + row * kDL * 2);
   const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + row * kDR * 2);
-  float amax = 0.f;
-  for (int c = lane; c < 72; c += 32) {
-    const uint4 v = c < 64 ? __ldg(qn + c) : __ldg(qp + (c - 64));
-    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+  // the row's 72 chunks of 16 bytes: all of a lane's loads in flight at once
+  uint4 v[3];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+  for (int k = 0; k < 3; ++k) {
+    const int c = lane + 32 * k;
+    v[k] = c < 64 ? __ldg(qn + c) : (c < 72 ? __ldg(qp + (c - 64)) : make_uint4(0u, 0u, 0u, 0u));
+  }
+  float amax = 0.f;  // zero chunks leave the maximum of |q| unchanged
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const uint32_t ws[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
       amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
     }
   }
