@@ -144,6 +144,19 @@ def test_combine_column_parts(lens_seed, H, Q, dtype):
     compare(wl, out, lse, label=f"combine parts B={n} H={H} Q={Q} {dtype}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_one_long_request_in_a_large_batch(dtype):
+    """64 requests, one of them 131,072 tokens long (cut over ~40 slices),
+    the rest 2,000: the batch is large enough that a warp merges a whole
+    row, and the long request's merge walks its pieces in column halves."""
+    lens = [2000] * 64
+    lens[17] = 131072
+    wl = W.custom(lens, num_heads=64, q_len=1, kv_dtype=dtype, seed=63)
+    out, lse, status, *_ = run_gpu(wl)
+    assert status == 0
+    compare(wl, out, lse, label=f"one long request in 64, {dtype}")
+
+
 def test_peaked_softmax():
     """q scaled x4: nearly one-hot weights, where the absolute tolerance term
     cannot hide errors."""
