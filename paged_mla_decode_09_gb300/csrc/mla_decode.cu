@@ -345,7 +345,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[k]), stream) == cudaSuccess;
   };
   if (!mark(0)) return MLA_ERR_CUDA;
-  mla::mla_schedule_kernel<<<1, 1024, 0, stream>>>(p);
+  mla::mla_schedule_kernel<<<1, (d->batch < 256 && C < 256) ? 256 : 1024, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
   if (f8) {  // per-row e4m3 query scales
     if (launch_pdl(mla::mla_qscale_kernel, dim3(static_cast<unsigned>((static_cast<int64_t>(d->batch) * R + 7) / 8)),

@@ -294,8 +294,11 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   __shared__ int32_t cnz[kSchedSmemC + 1];  // non-empty slices among clusters [0, c)
   __shared__ int32_t nsplit;
   __shared__ int32_t maxnp;
+  // 1024 threads, or 256 for a batch and a cluster count below 256 (fewer
+  // warps to gather at each barrier)
+  const int nt = static_cast<int>(blockDim.x), nwarps = nt >> 5;
   const bool sp_ok = p.B <= kSchedSmemB;
-  const bool c_ok = p.C <= kSchedSmemC;
+  const bool c_ok = p.C <= kSchedSmemC && p.C < nt;  // one cluster per thread
   griddep_launch_dependents();  // the next kernels wait for this one before reading its output
   const int tid = threadIdx.x;
 #ifdef MLA_TRACE
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   // this kernel, and every later writer waits for it (griddep_wait)
   if (tid < 4) p.status[tid] = 0;
   __syncthreads();
-  for (int base = 0; base < p.B; base += 1024) {
+  for (int base = 0; base < p.B; base += nt) {
     const int b = base + tid;
     int np = 0;
     if (b < p.B) {
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     if ((tid & 31) == 31) warp_tot[tid >> 5] = v;
     __syncthreads();
     if (tid < 32) {
-      int w = warp_tot[tid];
+      int w = tid < nwarps ? warp_tot[tid] : 0;
       for (int o = 1; o < 32; o <<= 1) {
         const int t = __shfl_up_sync(0xffffffffu, w, o);
         if (tid >= o) w += t;
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
       if (sp_ok) sp[b + 1] = incl;
     }
     __syncthreads();
-    if (tid == 1023) carry = incl;
+    if (tid == nt - 1) carry = incl;
     __syncthreads();
   }
   if (tid == 0) {
@@ -377,15 +380,22 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   // into pieces, so no partials are written and nothing is merged.
   const bool whole = p.B <= p.C && (static_cast<int64_t>(maxnp) + p.unit_cost) * p.C <=
                                        W + static_cast<int64_t>(kSplitPenaltyPages) * p.C;
-  for (int c = tid; c < p.C; c += 1024) {
+  // weighted cut positions W * c / C in 32-bit arithmetic when they fit
+  const bool cut32 = W * p.C < (static_cast<int64_t>(1) << 31);
+  auto cut = [&](int c) -> int64_t {
+    return cut32 ? static_cast<int64_t>(static_cast<uint32_t>(W) * static_cast<uint32_t>(c) /
+                                        static_cast<uint32_t>(p.C))
+                 : W * c / p.C;
+  };
+  for (int c = tid; c < p.C; c += nt) {
     int s, e, lo;
     if (whole) {  // slice c = request c; the slices past the batch are empty
       s = c < p.B ? pre[c] : static_cast<int>(T);
       e = c < p.B ? pre[c + 1] : static_cast<int>(T);
       lo = c < p.B ? c : p.B - 1;
     } else {
-      s = page_at(W * c / p.C);
-      e = page_at(W * (c + 1) / p.C);
+      s = page_at(cut(c));
+      e = page_at(cut(c + 1));
       lo = 0;
       int hi = p.B - 1;  // last request b with prefix[b] <= s
       while (lo < hi) {
@@ -402,8 +412,9 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
       cf[c] = lo;
     }
   }
-  // C <= 512: thread c wrote cluster c's slice; a ballot per warp of the
-  // non-empty ones, then each cluster's count of those before it
+  // C <= 512 and below the thread count: thread c wrote cluster c's slice;
+  // a ballot per warp of the non-empty ones, then each cluster's count of
+  // those before it
   const unsigned m = c_ok ? __ballot_sync(0xffffffffu, tid < p.C && cs[tid] != ce[tid]) : 0u;
   if (c_ok && (tid & 31) == 0) warp_tot[tid >> 5] = __popc(m);
   __syncthreads();
@@ -422,7 +433,7 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   // [prefix[b], prefix[b+1]): from the first with e > prefix[b] to the last
   // with s < prefix[b+1] (both bounds are non-decreasing in the cluster
   // index); the combine merges the pieces of requests with more than one
-  for (int b = tid; b < p.B; b += 1024) {
+  for (int b = tid; b < p.B; b += nt) {
     const int pb0 = pre[b], pb1 = pre[b + 1];
     int lo = 0, hi = p.C - 1;
     while (lo < hi) {
