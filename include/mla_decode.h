@@ -26,7 +26,10 @@
  *     the page table or the sequence lengths;
  *   - device pointers are CUDA device addresses on the current device;
  *     `stream` is a cudaStream_t passed as void* (NULL = legacy stream);
- *   - work is enqueued on `stream` and runs asynchronously;
+ *   - work is enqueued on `stream` and runs asynchronously; the call's last
+ *     kernel completes only after all of its earlier ones, so a kernel the
+ *     caller launches next on `stream` as a programmatic dependent sees all
+ *     of the call's output once its griddepcontrol.wait returns;
  *   - the return value is an mla_status; no C++ exception crosses the ABI;
  *   - errors that only the device can see (a page id outside the pool, a
  *     sequence length outside [q_len, max_pages_per_req * 64], a wait that

@@ -1598,9 +1598,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineBlocksPerSm) mla_c
   // row block y, rows 4(z / kParts) .. + 3 (one warp each).  The schedule
   // kernel ended before the attention kernel began, so its list is read
   // before waiting for the attention kernel (through L2: an earlier call's
-  // list may sit in this SM's L1); blocks past the list's end leave at once.
+  // list may sit in this SM's L1); blocks past the list's end leave at
+  // once, except block 0: it leaves only after the attention kernel has
+  // completed, so that this grid completes after every earlier kernel of the
+  // call even when nothing was cut (a kernel launched after the call as a
+  // programmatic dependent then sees all of its output after its own wait).
   const int nsplit = __ldcg(p.splits);
-  if (static_cast<int>(blockIdx.x) >= nsplit) return;
+  if (static_cast<int>(blockIdx.x) >= nsplit) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) griddep_wait();
+    return;
+  }
   uint32_t ent[8];
   ldcg_v8(p.splits + 8 * (1 + static_cast<int64_t>(blockIdx.x)), ent);
   griddep_wait();  // the attention kernel's partials are complete
