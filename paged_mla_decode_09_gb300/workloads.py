@@ -66,7 +66,7 @@ _CHUNK_PAGES = 256
 BF16_NAN = np.uint16(0x7FC0)
 E4M3_NAN = np.uint8(0x7F)
 
-CONFIG_NAMES = ("tiny", "kimi", "dsv3", "prefix", "fp8", "verify4", "dsa")
+CONFIG_NAMES = ("tiny", "kimi", "dsv3", "prefix", "fp8", "verify4", "dsa", "long")
 
 
 @dataclass
@@ -376,6 +376,16 @@ def make_config(name: str, seed: int | None = None, sentinel: str = "nan") -> Wo
         perm = rng.permutation(pool).astype(np.int32)
         table, _ = _tables_private(seq_lens, perm)
         return build(name, H, 4, seq_lens, table, pool, rng, seed, "bf16", sentinel=sentinel)
+    if name == "long":
+        # one long-context request (not one of the benchmark's batches): every
+        # slice of the work holds a piece of it, and the merge of 76 pieces
+        # per query row dominates the step outside the attention kernel
+        B, H, L = 1, 128, 131072
+        seq_lens = np.full(B, L, dtype=np.int32)
+        pool = B * (L // PAGE_SIZE)
+        perm = rng.permutation(pool).astype(np.int32)
+        table, _ = _tables_private(seq_lens, perm)
+        return build(name, H, 1, seq_lens, table, pool, rng, seed, "bf16", sentinel=sentinel)
     raise ValueError(name)
 
 
