@@ -285,7 +285,8 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
                 const int32_t* page_table, const int32_t* seq_lens, int32_t q_len, float scale, float kv_scale,
                 void* out, float* lse, uint8_t* ws, size_t ws_bytes, bool shrink_to_fit, int32_t* status_out,
                 void* stream_v, void* const* events, bool out_f32 = false, int32_t len_offset = 0,
-                int32_t len_fixed = 0) {
+                int32_t len_fixed = 0, const int32_t* topk_bits = nullptr, const int32_t* topk_empty = nullptr,
+                int32_t topk_nchunk = 0) {
   int rc = check_call(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse, status_out);
   if (rc != MLA_OK) return rc;
   if (!ws) return MLA_ERR_INVALID_ARG;
@@ -336,6 +337,9 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.out_f32 = out_f32 ? 1 : 0;
   p.len_offset = len_offset;
   p.len_fixed = len_fixed;
+  p.topk_bits = topk_bits;
+  p.topk_empty = topk_empty;
+  p.topk_nchunk = topk_nchunk;
   p.scale = scale;
   p.kv_scale = f8 ? kv_scale : 1.f;
   p.timeout_ns = kTimeoutNs;
@@ -466,6 +470,16 @@ int mla_decode_profiled(const mla_dims* d, const void* q_nope, const void* q_pe,
   if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return MLA_ERR_INVALID_ARG;
   return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, q_len, scale, kv_scale, out, lse,
                      static_cast<uint8_t*>(workspace), workspace_bytes, false, nullptr, stream, events);
+}
+
+int mla_decode_topk_packed(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
+                           const int32_t* page_table, const int32_t* seq_lens, float scale, float kv_scale, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes, const int32_t* gather_bits,
+                           int32_t gather_nchunk, const int32_t* list_empty, void* stream) {
+  if (!gather_bits || !list_empty || gather_nchunk < 1) return MLA_ERR_INVALID_ARG;
+  return decode_impl(d, q_nope, q_pe, kv_cache, page_table, seq_lens, 1, scale, kv_scale, out, lse,
+                     static_cast<uint8_t*>(workspace), workspace_bytes, false, nullptr, stream, nullptr, false, 0, 0,
+                     gather_bits, list_empty, gather_nchunk);
 }
 
 int mla_decode_f32_out(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,

@@ -224,6 +224,13 @@ struct Params {
   int32_t out_f32;         // out is fp32 [B][Q][H][512] instead of bf16 (internal: the cascade's passes)
   int32_t len_offset;      // request b's length is seq_lens[b] - len_offset (internal: the cascade's suffix pass)
   int32_t len_fixed;       // > 0: every request's length, seq_lens unread (internal: the cascade's prefix pass)
+  // internal, the top-k decode over packed pick lists (null otherwise): the
+  // gather's status bits, one word per (list, chunk of picks), are OR-ed into
+  // the status word by the schedule; a list without a valid pick gets the lse
+  // of an empty key set, -inf, from the combine's block 0
+  const int32_t* topk_bits;
+  const int32_t* topk_empty;  // [B]
+  int32_t topk_nchunk;
   float scale, kv_scale;
   uint64_t timeout_ns;
 };
@@ -313,6 +320,12 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
     nsplit = 0;
     maxnp = 0;
   }
+  // the top-k gather's status bits (it ended before this kernel began):
+  // loaded now, OR-ed into the status word at the end, so that the loads
+  // overlap the rest of the schedule
+  int topk_bits = 0;
+  if (p.topk_bits)
+    for (int64_t k = tid; k < static_cast<int64_t>(p.B) * p.topk_nchunk; k += nt) topk_bits |= p.topk_bits[k];
   // the status words start each call at zero: nothing writes them before
   // this kernel, and every later writer waits for it (griddep_wait)
   if (tid < 4) p.status[tid] = 0;
@@ -485,6 +498,10 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
   }
   __syncthreads();
   if (tid == 0) p.splits[0] = nsplit;
+  if (p.topk_bits) {
+    topk_bits = __reduce_or_sync(0xffffffffu, topk_bits);
+    if ((tid & 31) == 0 && topk_bits) atomicOr(p.status, topk_bits);
+  }
 #ifdef MLA_TRACE
   __syncthreads();
   if (tid == 0) g_mla_kernel_times[1] = globaltimer_ns();
@@ -1603,14 +1620,29 @@ __global__ void __launch_bounds__(kCombineWarps * 32, kCombineBlocksPerSm) mla_c
   // completed, so that this grid completes after every earlier kernel of the
   // call even when nothing was cut (a kernel launched after the call as a
   // programmatic dependent then sees all of its output after its own wait).
+  const bool block0 = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  // the lse of the top-k lists without a valid pick (their decode saw one
+  // all-zero key: out = 0 exactly), after the attention kernel wrote theirs
+  auto empty_lists = [&]() {  // one list per thread: a flag load, then its H stores if set
+    if (!p.topk_empty) return;
+    for (int bq = threadIdx.x; bq < p.B; bq += blockDim.x) {
+      if (!p.topk_empty[bq]) continue;
+      float* l = p.lse + static_cast<int64_t>(bq) * p.H;
+      for (int h = 0; h < p.H; ++h) l[h] = -INFINITY;
+    }
+  };
   const int nsplit = __ldcg(p.splits);
   if (static_cast<int>(blockIdx.x) >= nsplit) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) griddep_wait();
+    if (block0) {
+      griddep_wait();
+      empty_lists();
+    }
     return;
   }
   uint32_t ent[8];
   ldcg_v8(p.splits + 8 * (1 + static_cast<int64_t>(blockIdx.x)), ent);
   griddep_wait();  // the attention kernel's partials are complete
+  if (block0) empty_lists();
 #ifdef MLA_TRACE
   if (threadIdx.x == 0) atomicMin(&g_mla_kernel_times[2], globaltimer_ns());
   struct Exit {  // every warp stamps its exit (warps leave at different points)

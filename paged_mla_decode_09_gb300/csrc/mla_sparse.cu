@@ -6,7 +6,8 @@
 // Workspace: [per-block status bits | packed lengths | empty flags | packed
 // page table | packed rows | decode workspace].  The gather's blocks each
 // write their status bits to a word of their own (no word needs clearing
-// first); the closing kernel ORs them into the decode's status word.
+// first); the decode's schedule kernel ORs them into its status word, and
+// its combine kernel gives the lists without a valid entry lse = -inf.
 // Packed request b' = b * q_len + i owns pages b' * P .. b' * P + P - 1,
 // P = ceil(topk / 64), and its k-th valid entry is its packed row k.
 #include <cuda_runtime.h>
@@ -16,6 +17,7 @@
 #include <cstdint>
 
 #include "mla_decode.h"
+#include "mla_internal.h"
 #include "mla_sparse.h"
 
 namespace {
@@ -153,24 +155,6 @@ __global__ void __launch_bounds__(kChunkEntries)
   if (threadIdx.x == 0) block_bits[static_cast<int64_t>(bq) * gridDim.x + chunk] = bits;
 }
 
-// After the decode, one warp per packed request: ORs the gather blocks'
-// status bits of the request into the decode's status word, and gives a
-// (b, i) whose list held no valid entry (decoded over one all-zero key,
-// which leaves out = 0 exactly) the lse of an empty key set, -inf.
-__global__ void __launch_bounds__(256) mla_topk_finish_kernel(const int32_t* __restrict__ block_bits, int nchunk,
-                                                              const int32_t* __restrict__ packed_empty, int bq_total,
-                                                              int H, float* __restrict__ lse, int32_t* status) {
-  const int bq = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (bq >= bq_total) return;
-  int bits = 0;
-  for (int c = lane; c < nchunk; c += 32) bits |= block_bits[static_cast<int64_t>(bq) * nchunk + c];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, o);
-  if (lane == 0 && bits) atomicOr(status, bits);
-  if (!packed_empty[bq]) return;
-  for (int h = lane; h < H; h += 32) lse[static_cast<int64_t>(bq) * H + h] = -INFINITY;
-}
-
 }  // namespace mla
 
 namespace {
@@ -266,15 +250,11 @@ int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, c
         d->page_table_stride, pd.max_pages_per_req, rows, ppt, plen, pempty, block_bits);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
   // the packed problem: request b * q_len + i has one draft position; its
-  // queries and outputs are those of (b, i), already laid out that way
-  const int rc = mla_decode(&pd, q_nope, q_pe, rows, ppt, plen, 1, scale, kv_scale, out, lse, ws + l.dec,
-                            workspace_bytes - l.dec, stream_v);
-  if (rc != MLA_OK) return rc;
-  // the decode's status word (cleared by its schedule kernel) collects the gather's bits too
-  mla::mla_topk_finish_kernel<<<(pd.batch + 7) / 8, 256, 0, stream>>>(
-      block_bits, static_cast<int>(grid.x), pempty, pd.batch, d->num_heads, lse,
-      reinterpret_cast<int32_t*>(ws + l.dec));
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  // queries and outputs are those of (b, i), already laid out that way.  The
+  // decode's status word (cleared by its schedule kernel) collects the
+  // gather's bits too, and lists without a valid pick get lse = -inf.
+  return mla_decode_topk_packed(&pd, q_nope, q_pe, rows, ppt, plen, scale, kv_scale, out, lse, ws + l.dec,
+                                workspace_bytes - l.dec, block_bits, static_cast<int32_t>(grid.x), pempty, stream_v);
 }
 
 int mla_decode_sparse_query_status(const mla_dims* d, int32_t topk, const void* workspace, void* stream_v,
