@@ -888,7 +888,7 @@ def run_sparse(args):
             "e2e": {"value": job_picked / (e2e_ms * 1e-3), "unit": "picked-KV-tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             # gather, schedule, attention, combine
-            "gpu_launches": 5 * args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
+            "gpu_launches": 4 * args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
         }))
     if world > 1:
         torch.distributed.destroy_process_group()
