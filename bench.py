@@ -1011,8 +1011,8 @@ def run_cascade(args):
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": job_tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            # prep, prefix pass (schedule, attention, combine), status, suffix pass (3), status, merge
-            "gpu_launches": 10 * args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
+            # prefix pass (schedule, attention, combine), suffix pass (the same three), merge
+            "gpu_launches": 7 * args.steps, "clocks": clk.summary(), "device_status": st, "parity_sample": parity,
         }))
     if world > 1:
         torch.distributed.destroy_process_group()
