@@ -994,7 +994,7 @@ def run_cascade(args):
     else:
         roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": bf16_peak, "unit": "TFLOP/s"}
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "peak_source": peak_src,
-                 "kernel": "cascade step (prep, prefix decode, suffix decode, merge)", "alg_bytes": nbytes,
+                 "kernel": "cascade step (prefix decode, suffix decode, merge)", "alg_bytes": nbytes,
                  "alg_flops": flops})
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
