@@ -41,13 +41,13 @@ cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t sm
 // Workspace: [status words | page prefix sums | cluster slices | each
 // request's first and last cluster | the requests cut into pieces, each with
 // its pieces' partial slots | fp32 partial outputs | partial log-sum-exps |
-// e4m3 query scales].  Sized by B, the cluster count and the number of row
-// blocks only.
+// e4m3 query scales | e4m3 query terms (1152 bytes a row)].  Sized by B,
+// the cluster count, the number of row blocks and the cache type only.
 struct Layout {
-  size_t status, prefix, cinfo, rrange, splits, o_part, lse_part, qscale, total;
+  size_t status, prefix, cinfo, rrange, splits, o_part, lse_part, qscale, qterms, total;
 };
 
-Layout workspace_layout(int B, int C, int G) {
+Layout workspace_layout(int B, int C, int G, bool qterms) {
   Layout l;
   l.status = 0;
   l.prefix = 256;
@@ -57,7 +57,8 @@ Layout workspace_layout(int B, int C, int G) {
   l.o_part = l.splits + align256(static_cast<size_t>(1 + (B < C ? B : C)) * 8 * 4);
   l.lse_part = l.o_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * mla::kDL * 4);
   l.qscale = l.lse_part + align256(static_cast<size_t>(2 * C) * G * mla::kRows * 4);
-  l.total = l.qscale + align256(static_cast<size_t>(B) * G * mla::kRows * 4);  // e4m3 query scales
+  l.qterms = l.qscale + align256(static_cast<size_t>(B) * G * mla::kRows * 4);  // e4m3 query scales
+  l.total = l.qterms + (qterms ? align256(static_cast<size_t>(B) * G * mla::kRows * 1152) : 0);
   return l;
 }
 
@@ -113,10 +114,12 @@ int launch_shape(int device, bool f8, int G, int* clusters_out) {
   int rc = device_ok(device);
   int n = 0;
   if (rc == MLA_OK) {
-    const void* fn = f8 ? reinterpret_cast<const void*>(&mla::mla_decode_kernel<true>)
-                        : reinterpret_cast<const void*>(&mla::mla_decode_kernel<false>);
+    const void* fn = f8 ? reinterpret_cast<const void*>(&mla::mla_decode_kernel<true, true>)
+                        : reinterpret_cast<const void*>(&mla::mla_decode_kernel<false, false>);
     const int smem = f8 ? Cfg<true>::kSmem : Cfg<false>::kSmem;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        (f8 && cudaFuncSetAttribute(reinterpret_cast<const void*>(&mla::mla_decode_kernel<true, false>),
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)) {
       rc = MLA_ERR_CUDA;
     } else {
       cudaLaunchConfig_t cfg = {};
@@ -232,10 +235,25 @@ int make_maps(const void* kv, int num_pages, bool f8, Maps* m) {
 
 // Query rows as copied into the S CTA's ring (64 rows per copy, laid out
 // like a page): q_nope as 8 boxes of 64 values, q_pe as one.
-int make_qmaps(const void* q_nope, const void* q_pe, int64_t rows, Maps* m) {
+// Tensor maps of the queries: q_nope as 8 boxes and q_pe as one box of 64
+// rows (the bf16 S CTA's ring entries).  With e4m3 query terms the first map
+// instead covers the terms, [rows][1152] bytes read as 9 boxes of 128 bytes
+// of 32 rows (36 KB, an e4m3 ring slot).
+int make_qmaps(const void* q_nope, const void* q_pe, const uint8_t* qterms, int64_t rows, Maps* m) {
   auto enc = encode_fn();
   if (!enc) return MLA_ERR_CUDA;
   cuuint32_t estr[3] = {1, 1, 1};
+  if (qterms) {
+    cuuint64_t gdim[3] = {128, static_cast<cuuint64_t>(rows), 9};
+    cuuint64_t gstr[2] = {1152, 128};
+    cuuint32_t box[3] = {128, 32, 9};
+    const CUresult r = enc(&m->qn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(qterms), gdim, gstr, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+    m->qp = m->qn;  // unused with terms
+    return MLA_OK;
+  }
   cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(rows), 8};
   cuuint64_t gstr[2] = {1024, 128};
   cuuint32_t box[3] = {64, 64, 8};
@@ -299,15 +317,20 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   const int G = (R + mla::kRows - 1) / mla::kRows;
   int C = 0;
   if ((rc = launch_shape(dev, f8, G, &C)) != MLA_OK) return rc;
+  // e4m3: the query terms prepared by the scale pre-pass when the workspace
+  // has room for them, else the attention kernel splits the rows itself
+  bool terms = f8 && workspace_layout(d->batch, C, G, true).total <= ws_bytes;
   if (shrink_to_fit) {
-    while (C > 0 && workspace_layout(d->batch, C, G).total > ws_bytes) --C;
+    while (C > 0 && workspace_layout(d->batch, C, G, terms).total > ws_bytes) --C;
     if (C < 1) return MLA_ERR_SCRATCH_TOO_SMALL;
   }
-  const Layout lay = workspace_layout(d->batch, C, G);
+  const Layout lay = workspace_layout(d->batch, C, G, terms);
   if (ws_bytes < lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   Maps maps;
   if ((rc = make_maps(kv_cache, d->num_pages, f8, &maps)) != MLA_OK) return rc;
-  if ((rc = make_qmaps(q_nope, q_pe, static_cast<int64_t>(d->batch) * R, &maps)) != MLA_OK) return rc;
+  if ((rc = make_qmaps(q_nope, q_pe, terms ? ws + lay.qterms : nullptr, static_cast<int64_t>(d->batch) * R, &maps)) !=
+      MLA_OK)
+    return rc;
 
   Params p;
   p.q_nope = static_cast<const uint8_t*>(q_nope);
@@ -324,6 +347,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.rrange = reinterpret_cast<int32_t*>(ws + lay.rrange);
   p.splits = reinterpret_cast<int32_t*>(ws + lay.splits);
   p.qscale = reinterpret_cast<float*>(ws + lay.qscale);
+  p.qterms = terms ? ws + lay.qterms : nullptr;
   p.B = d->batch;
   p.H = d->num_heads;
   p.Q = d->q_len;
@@ -374,9 +398,11 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true>, p, maps.s, maps.o, maps.pe, maps.qn,
-                                          maps.qp)
-                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false>, p, maps.s, maps.o, maps.pe,
+  cudaError_t e = f8 ? (terms ? cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true, true>, p, maps.s, maps.o,
+                                                     maps.pe, maps.qn, maps.qp)
+                             : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<true, false>, p, maps.s, maps.o,
+                                                     maps.pe, maps.qn, maps.qp))
+                     : cudaLaunchKernelEx(&cfg, mla::mla_decode_kernel<false, false>, p, maps.s, maps.o, maps.pe,
                                           maps.qn, maps.qp);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -453,7 +479,7 @@ size_t mla_decode_workspace_size(const mla_dims* d, int device) {
   const int G = (d->num_heads * d->q_len + mla::kRows - 1) / mla::kRows;
   int C = 0;
   if (launch_shape(device, d->kv_dtype == MLA_KV_FP8_E4M3, G, &C) != MLA_OK) return 0;
-  return workspace_layout(d->batch, C, G).total;
+  return workspace_layout(d->batch, C, G, d->kv_dtype == MLA_KV_FP8_E4M3).total;
 }
 
 int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,

@@ -218,6 +218,11 @@ struct Params {
   int32_t* splits;         // [8] count, then [min(B, C)][8] = (request, pieces, partial slots of the first 6)
                            // for each request cut into pieces (any order)
   float* qscale;           // [B * R] e4m3 query scales (e4m3 cache only)
+  // e4m3 cache: [B * R][1152] each query row's e4m3 terms, hi (576 bytes)
+  // then lo, written by the scale pre-pass and copied into the S CTA's ring
+  // like the bf16 query rows; null: the attention kernel splits the rows
+  // itself (the allocation-free entry point when they do not fit its scratch)
+  uint8_t* qterms;
   int32_t B, H, Q, R, G, C;
   int32_t num_pages, max_pages, pt_stride;
   int32_t unit_cost;       // schedule weight of a request piece, in pages
@@ -510,7 +515,19 @@ __global__ void __launch_bounds__(1024) mla_schedule_kernel(Params p) {
 
 // ---------------------------------------------------------------- K0b
 // e4m3 cache: per query row r of request b, the scale of its e4m3 split,
-// max |q| / 448 over the 576 values (1 for an all-zero row).  One warp per row.
+// max |q| / 448 over the 576 values (1 for an all-zero row), and (with
+// p.qterms) the split itself: hi = e4m3(q / scale), lo = e4m3(q / scale -
+// hi), 576 codes each, the same arithmetic as the attention kernel's own
+// split.  One warp per row.
+__device__ __forceinline__ void e4m3_split_pair(float2 x, uint32_t& hi16, uint32_t& lo16) {
+  const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+  const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  const __nv_fp8x2_storage_t l = __nv_cvt_float2_to_fp8x2(make_float2(x.x - hf.x, x.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+  hi16 = h;
+  lo16 = l;
+}
+
 __global__ void __launch_bounds__(256) mla_qscale_kernel(Params p) {
   // needs nothing from the schedule, so it may run beside it; block 0 ends
   // only after the schedule has (griddep_wait below), so the attention
@@ -545,7 +562,31 @@ __global__ void __launch_bounds__(256) mla_qscale_kernel(Params p) {
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if (lane == 0) p.qscale[row] = amax > 0.f ? amax / 448.f : 1.f;
+  const float qs = amax > 0.f ? amax / 448.f : 1.f;  // every lane holds the row's max
+  if (lane == 0) p.qscale[row] = qs;
+  if (p.qterms) {  // chunk c (8 values) -> 8 hi codes at 8c, 8 lo codes at 576 + 8c
+    const float inv = 1.f / qs;
+    uint8_t* t = p.qterms + row * 1152;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int c = lane + 32 * k;
+      if (c >= 72) continue;
+      const uint32_t ws[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      uint32_t hi[2], lo[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[2 * h2]));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[2 * h2 + 1]));
+        uint32_t h0, l0, h1, l1;
+        e4m3_split_pair(make_float2(f0.x * inv, f0.y * inv), h0, l0);
+        e4m3_split_pair(make_float2(f1.x * inv, f1.y * inv), h1, l1);
+        hi[h2] = (h0 & 0xFFFFu) | (h1 << 16);
+        lo[h2] = (l0 & 0xFFFFu) | (l1 << 16);
+      }
+      *reinterpret_cast<uint2*>(t + 8 * c) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(t + 576 + 8 * c) = make_uint2(lo[0], lo[1]);
+    }
+  }
   if (blockIdx.x == 0) griddep_wait();
 }
 
@@ -624,6 +665,13 @@ __device__ __forceinline__ int32_t read_page_id(const Params& p, int b, int pg) 
 // Ring entries of the bf16 S CTA holding a unit's query rows: 64 rows per
 // entry, laid out like a page (8 boxes of q_nope, the 9th of q_pe).
 __device__ __forceinline__ int q_entries(int rows_real) { return (rows_real + 63) / 64; }
+// Ring entries of the S CTA holding a unit's query rows: bf16, 64 rows per
+// entry; e4m3 terms (hi + lo, 1152 bytes a row like bf16), 32 rows per
+// 36 KB entry (kQT); none when the e4m3 kernel splits the rows itself.
+template <bool kF8, bool kQT>
+__device__ __forceinline__ int q_entries_of(int rows_real) {
+  return kF8 ? (kQT ? (rows_real + 31) / 32 : 0) : q_entries(rows_real);
+}
 
 // TMA producer shared by both roles: streams the slice's pages into a ring
 // of kNSt slots (entry i: slot i % kNSt, phase (i / kNSt) & 1).  The bf16 S
@@ -631,7 +679,7 @@ __device__ __forceinline__ int q_entries(int rows_real) { return (rows_real + 63
 // (q_entries entries), which the softmax warps move into TMEM: coalesced
 // copies issued as soon as a slot frees, instead of per-row loads at the
 // unit boundary.
-template <bool kF8, bool kRoleS>
+template <bool kF8, bool kQT, bool kRoleS>
 __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const CUtensorMap* tm_kv,
                              const CUtensorMap* tm_pe, const CUtensorMap* tm_qn, const CUtensorMap* tm_qp, int cid,
                              int g, uint32_t partner) {
@@ -641,7 +689,7 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
   constexpr uint32_t kCopyBytes = static_cast<uint32_t>((kRoleS ? C::kBoxesPartS : C::kBoxesPartO) * C::kBox);
   volatile int* abort = &ctrl->abort;
   const int rows_real = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
-  const int qe = (kRoleS && !kF8) ? q_entries(rows_real) : 0;
+  const int qe = kRoleS ? q_entries_of<kF8, kQT>(rows_real) : 0;
   UnitIter it;
   it.init(p, cid);
   Unit u;
@@ -683,10 +731,10 @@ __device__ void run_producer(const Params& p, Ctrl* ctrl, uint8_t* ring, const C
         ok = false;
         break;
       }
-      const int row = static_cast<int>(static_cast<int64_t>(u.b) * p.Q * p.H + g * kRows + 64 * e);
+      const int row = static_cast<int>(static_cast<int64_t>(u.b) * p.Q * p.H + g * kRows + (kF8 ? 32 : 64) * e);
       mbar_expect_tx(bar, static_cast<uint32_t>(C::kSlotS));
-      tma_load_3d(smem_u32(slot), tm_qn, 0, row, 0, bar);
-      tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_qp, 0, row, bar);
+      tma_load_3d(smem_u32(slot), tm_qn, 0, row, 0, bar);  // e4m3: the 9 boxes of 32 rows of terms
+      if constexpr (!kF8) tma_load_2d(smem_u32(slot + C::kNBoxLat * C::kBox), tm_qp, 0, row, bar);
       ++i;
     }
     for (int pg = u.p0; pg < u.p1 && ok; ++pg, ++j) {
@@ -911,10 +959,13 @@ __device__ __forceinline__ float load_q_row(const Params& p, int b, int g, int r
   }
 }
 
-// bf16 query row from a ring entry into TMEM lane r: 16-byte chunks
-// [c0, c0 + 36) (chunk c = box c / 8 (8 of q_nope, then q_pe), piece c % 8 of
-// the 128-byte-swizzled row rq).  src = the row's first box row, or null
-// for a padding row (zeros).
+// A query row from a ring entry into TMEM lane r: 16-byte chunks [c0, c0 +
+// 36) (chunk c = box c / 8, piece c % 8 of the 128-byte-swizzled row rq;
+// boxes of kBoxBytes).  bf16: 8 boxes of q_nope, then q_pe, 2 values a
+// column; e4m3: the row's hi term then its lo term, 4 codes a column, so the
+// lo term starts at column 144.  src = the row's first box row, or null for
+// a padding row (zeros).
+template <int kBoxBytes>
 __device__ __forceinline__ void load_q_row_smem(const uint8_t* src, int rq, uint32_t taddr_row, int c0) {
 #pragma unroll
   for (int c = 0; c < 36; c += 12) {
@@ -922,7 +973,7 @@ __device__ __forceinline__ void load_q_row_smem(const uint8_t* src, int rq, uint
 #pragma unroll
     for (int k = 0; k < 12; ++k) {
       const int cc = c0 + c + k;
-      v[k] = src ? *reinterpret_cast<const uint4*>(src + (cc >> 3) * 8192 + (((cc & 7) ^ (rq & 7)) << 4))
+      v[k] = src ? *reinterpret_cast<const uint4*>(src + (cc >> 3) * kBoxBytes + (((cc & 7) ^ (rq & 7)) << 4))
                  : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
@@ -938,7 +989,10 @@ __device__ __forceinline__ void load_q_row_smem(const uint8_t* src, int rq, uint
 }
 
 // ---------------------------------------------------------------- K1
-template <bool kF8>
+// kQT (e4m3 only): the query terms come from the scale pre-pass through the
+// ring (p.qterms), else the softmax warps split the bf16 rows themselves;
+// separate instantiations, so that neither path's registers burden the other.
+template <bool kF8, bool kQT>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_s,
                       const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_pe,
@@ -1017,7 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =========================== S CTA ===========================
     uint8_t* ring = data;
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, true>(p, ctrl, ring, &tm_s, &tm_pe, &tm_qn, &tm_qp, cid, g, partner);
+      if (lane == 0) run_producer<kF8, kQT, true>(p, ctrl, ring, &tm_s, &tm_pe, &tm_qn, &tm_qp, cid, g, partner);
     } else if (warp == 1) {
       // QK issuer: the whole warp runs the loop and one elected lane issues
       // (a converged warp keeps the tensor pipe full with N = 64 MMAs), so
@@ -1028,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t j = 0, un = 0;
       bool ok = true;
       int why = 0;
-      const int qe = kF8 ? 0 : q_entries(p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
+      const int qe = q_entries_of<kF8, kQT>(p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
       while (ok && it.next(u)) {
         if (!mbar_wait_warp(smem_u32(&ctrl->q_full), un & 1, abort, p.timeout_ns)) {
           ok = false;
@@ -1123,7 +1177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool real = rr < p.R;  // rows past H * q_len are padding: nothing of theirs is sent
       const PSlots ps(kF8, p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
       const int qi = real ? rr / p.H : p.Q - 1;
-      const int qe = kF8 ? 0 : q_entries(p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
+      const int qe = q_entries_of<kF8, kQT>(p.R - g * kRows < kRows ? p.R - g * kRows : kRows);
       UnitIter it;
       it.init(p, cid);
       Unit u;
@@ -1146,12 +1200,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (r == 0 && gg == 0) MLA_TRACE_POINT(0, 12, un);
-          if constexpr (kF8) {
+          if constexpr (kF8 && !kQT) {
             if (gg == 0) load_q_row<true, 32>(p, u.b, g, r, tmem + lane_base, 0, qs);
             else load_q_row<true, 40>(p, u.b, g, r, tmem + lane_base, 32, qs);
           } else {
-            // the producer copied this unit's query rows into ring entries
-            // j + qe * un ..; half gg moves chunks [36 gg, 36 gg + 36) of row r
+            // the producer copied this unit's query rows (e4m3: their terms)
+            // into ring entries j + qe * un ..; half gg moves chunks
+            // [36 gg, 36 gg + 36) of row r (e4m3: the hi, then the lo term)
             const uint32_t iq = j + qe * un;
             bool got = true;
             for (int e = 0; e < qe && got; ++e)
@@ -1162,9 +1217,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               why = kWaitQEntry;
               break;
             }
-            const int e = r >> 6, rq = r & 63;
+            constexpr int kEntryRows = kF8 ? 32 : 64;
+            const int e = r / kEntryRows, rq = r % kEntryRows;
             const uint8_t* src = (real && e < qe) ? ring + ((iq + e) % C::kNStS) * C::kSlotS + rq * 128 : nullptr;
-            load_q_row_smem(src, rq, tmem + lane_base, 36 * gg);
+            load_q_row_smem<kEntryRows * 128>(src, rq, tmem + lane_base, 36 * gg);
           }
           tc_fence_before();
           __syncwarp();
@@ -1364,7 +1420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows_real = p.R - g * kRows < kRows ? p.R - g * kRows : kRows;
     const PSlots ps(kF8, rows_real);
     if (warp == 0) {
-      if (lane == 0) run_producer<kF8, false>(p, ctrl, ring, &tm_o, &tm_pe, &tm_qn, &tm_qp, cid, g, partner);
+      if (lane == 0) run_producer<kF8, kQT, false>(p, ctrl, ring, &tm_o, &tm_pe, &tm_qn, &tm_qp, cid, g, partner);
     } else if (warp == 1) {
       // ---- PV warp: for page j it waits until the page is ready for PV
       // (c_kv landed, P arrived, O free on a unit's first page: the

@@ -157,6 +157,38 @@ def test_one_long_request_in_a_large_batch(dtype):
     compare(wl, out, lse, label=f"one long request in 64, {dtype}")
 
 
+@pytest.mark.parametrize("seq_lens,H,Q", [
+    ([2048, 5000, 1100], 128, 2),   # two row blocks per request
+    ([1500, 4100, 3], 16, 2),       # 32 rows: one 32-row query entry
+    ([700, 129, 64, 9000], 64, 1),  # 64 rows: two entries
+])
+def test_e4m3_query_terms_match_in_kernel_split(seq_lens, H, Q):
+    """e4m3: the query terms prepared by the scale pre-pass (a workspace with
+    room for them) and the attention kernel's own split of the bf16 rows (a
+    workspace without it) give bit-identical results, and match the oracle."""
+    import paged_mla_decode_09_gb300 as mla
+    from paged_mla_decode_09_gb300.device_inputs import out_to_f64, to_device
+
+    wl = W.custom(seq_lens, num_heads=H, q_len=Q, kv_dtype="fp8_e4m3", seed=71 + H)
+    db = to_device(wl, "cuda")
+    bufs = mla.alloc_buffers(db.q_nope, db.kv_cache, db.page_table)
+    G = -(-(H * Q) // 128)
+    terms_bytes = -(-(wl.batch * G * 128 * 1152) // 256) * 256  # the last region of the workspace
+    res = []
+    for ws in (bufs.workspace, bufs.workspace[: bufs.workspace.numel() - terms_bytes]):
+        bufs.out.fill_(float("nan"))
+        bufs.lse.fill_(float("nan"))
+        ws.fill_(0xFF)
+        mla.mla_decode(db.q_nope, db.q_pe, db.kv_cache, db.page_table, db.seq_lens, db.q_len, db.scale,
+                       db.kv_scale, bufs.out, bufs.lse, ws)
+        torch.cuda.synchronize()
+        assert mla.mla_query_status(ws) == 0
+        res.append((bufs.out.clone(), bufs.lse.clone()))
+    assert torch.equal(res[0][0].view(torch.int16), res[1][0].view(torch.int16))
+    assert torch.equal(res[0][1], res[1][1])
+    compare(wl, out_to_f64(res[0][0]), res[0][1].cpu().numpy().astype(np.float64), label=f"terms {seq_lens} H={H}")
+
+
 def test_peaked_softmax():
     """q scaled x4: nearly one-hot weights, where the absolute tolerance term
     cannot hide errors."""
