@@ -85,15 +85,20 @@ typedef struct {
 
 /*
  * Bytes of workspace mla_decode needs for these dimensions on `device`.
- * Depends on the dimensions and the device's SM count only, never on the
- * values in seq_lens, so one allocation serves every step of a batch shape.
- * Returns 0 on invalid dimensions or if the device cannot be queried.
+ * Depends on the dimensions (cache type included) and the device's SM count
+ * only, never on the values in seq_lens, so one allocation serves every step
+ * of a batch shape.  With an e4m3 cache it includes 1152 bytes per query row
+ * (128 per row block at least) for the queries' e4m3 terms; a workspace
+ * without room for them still works, with the attention kernel splitting the
+ * queries itself, more slowly.  Returns 0 on invalid dimensions or if the
+ * device cannot be queried.
  */
 size_t mla_decode_workspace_size(const mla_dims* d, int device);
 
 /*
  * One decode step: three kernels on `stream` (schedule, split-KV attention,
- * log-sum-exp combine).
+ * log-sum-exp combine; with an e4m3 cache a fourth, the queries' scales and
+ * e4m3 terms, beside the schedule).
  *
  *   q_nope      bf16 [B][q_len][H][512], contiguous, 32-byte aligned
  *   q_pe        bf16 [B][q_len][H][64],  contiguous, 32-byte aligned
@@ -110,7 +115,8 @@ size_t mla_decode_workspace_size(const mla_dims* d, int device);
  *               32 bytes per access)
  *   lse         fp32 [B][q_len][H], natural log of sum exp(score)
  *   workspace   >= mla_decode_workspace_size bytes, 256-byte aligned device memory;
- *               holds the status words, the schedule and fp32 split partials;
+ *               holds the status words, the schedule, fp32 split partials and
+ *               (e4m3 cache) the queries' scales and e4m3 terms;
  *               must not be shared by calls that may run concurrently
  */
 int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const void* kv_cache,
@@ -181,7 +187,12 @@ int mla_selftest_wait_timeout(void* workspace, uint32_t timeout_us, void* stream
  *     as fast as mla_decode.  Larger batches leave less room for partials
  *     and are decoded on fewer slices, more slowly; if even one slice's
  *     partials do not fit (very large batches), the call returns
- *     MLA_ERR_SCRATCH_TOO_SMALL.
+ *     MLA_ERR_SCRATCH_TOO_SMALL.  With an e4m3 cache the queries' e4m3
+ *     terms (147 KB per request and row block) are prepared in the array
+ *     only when they fit beside the full partials (about a dozen requests
+ *     on GB300); otherwise
+ *     the attention kernel splits the queries itself, as fast as mla_decode
+ *     with a workspace without room for the terms.
  *   - All calls share the one array, which keeps the last call's contents:
  *     calls that may overlap on the GPU (other streams, other threads)
  *     race and must be serialised by the caller.
