@@ -357,7 +357,7 @@ int decode_impl(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   p.num_pages = d->num_pages;
   p.max_pages = d->max_pages_per_req;
   p.pt_stride = d->page_table_stride;
-  p.unit_cost = mla::unit_cost_pages(f8, R < mla::kRows ? R : mla::kRows, terms);
+  p.unit_cost = mla::unit_cost_pages(f8, R < mla::kRows ? R : mla::kRows);
   p.out_f32 = out_f32 ? 1 : 0;
   p.len_offset = len_offset;
   p.len_fixed = len_fixed;

@@ -60,11 +60,12 @@ constexpr int kCtrlBytes = 512;
 // epilogue).  Measured on GB300 (per-cluster times regressed on the pages
 // and pieces of their slices, and sweeps): about 6 pages' time for a block
 // of 128 rows, 3-4 for one of at most 64 rows (half the queries to load and
-// half the output to store); with e4m3, 6 when the scale pre-pass prepared
-// the query terms, 10 when the attention kernel splits the rows itself at
-// each piece's start.
-__host__ __device__ constexpr int unit_cost_pages(bool f8, int block_rows, bool qterms) {
-  return f8 ? (qterms ? 6 : 10) : (block_rows <= 64 ? 4 : 6);
+// half the output to store).  With e4m3, 6 was best when the scale pre-pass
+// prepares the query terms; when the attention kernel splits the rows
+// itself the step was flat within 0.3 % from 8 to 14, and the same 6 keeps
+// both query paths on one schedule (bit-identical results).
+__host__ __device__ constexpr int unit_cost_pages(bool f8, int block_rows) {
+  return f8 ? 6 : (block_rows <= 64 ? 4 : 6);
 }
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
